@@ -287,4 +287,4 @@ def expert_counts(topk_ids: np.ndarray, num_experts: int) -> np.ndarray:
 
 
 __all__.append("expert_counts")
-__all__.append("SWEEP_TOKENS")
+__all__ += ["SWEEP_TOKENS", "SCALE_LO", "SCALE_HI", "GROUP"]

@@ -1,0 +1,126 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument checks reject bad calls before any CUDA work (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe_w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_moe_w4a16_build", os.path.join(ROOT, "w4a16_int4_mixture_grouped_gb300", "build.py"))
+    B = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(B)
+    path = B.build()
+    return ctypes.CDLL(path)
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^MOE_W4A16_API\s+[\w\s\*]+?\b(moe_w4a16_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for required in ("moe_w4a16_prepare", "moe_w4a16_indexed", "moe_w4a16_contiguous", "moe_w4a16_masked",
+                     "moe_w4a16_align", "moe_w4a16_dequant_check"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    lib.moe_w4a16_status_string.restype = ctypes.c_char_p
+    for s in range(9):
+        assert lib.moe_w4a16_status_string(s)
+    assert lib.moe_w4a16_status_string(99) == b"unknown status"
+    lib.moe_w4a16_abi_version.restype = ctypes.c_uint32
+    assert lib.moe_w4a16_abi_version() == 1
+
+
+def test_prepare_size_schema_checks(lib):
+    f = lib.moe_w4a16_prepare_size
+    out = ctypes.c_size_t(0)
+    assert f(384, 4096, 7168, 32, 1, ctypes.byref(out)) == 0
+    assert out.value == 256 + 384 * (4096 // 128) * (7168 // 64) * 4608
+    assert f(8, 256, 512, 64, 1, ctypes.byref(out)) == 2      # group 64: unsupported scheme, fails at load
+    assert f(8, 256, 500, 32, 1, ctypes.byref(out)) == 2      # K % 64 != 0
+    assert f(8, 200, 512, 32, 1, ctypes.byref(out)) == 2      # N % 256 != 0
+    assert f(8, 256, 512, 32, 7, ctypes.byref(out)) == 1      # unknown mode
+    assert f(0, 256, 512, 32, 1, ctypes.byref(out)) == 1
+    assert f(2000, 256, 512, 32, 1, ctypes.byref(out)) == 1   # more than 1024 experts
+
+
+def test_align_size_capacity(lib):
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.moe_w4a16_align_size(64, 8, 384, 32, ctypes.byref(a), ctypes.byref(b)) == 0
+    cap = 512 + 384 * 31
+    cap = -(-cap // 32) * 32
+    assert a.value == cap and b.value == cap // 32
+    assert lib.moe_w4a16_align_size(64, 8, 384, 257, ctypes.byref(a), ctypes.byref(b)) == 1
+
+
+def test_workspace_size(lib):
+    out = ctypes.c_size_t(0)
+    assert lib.moe_w4a16_workspace_size(128, 8, 7168, 0, ctypes.byref(out)) == 0 and out.value == 256
+    assert lib.moe_w4a16_workspace_size(128, 8, 7168, 2, ctypes.byref(out)) == 0
+    counters = -(-(128 * 28 * 8 * 4) // 256) * 256
+    y = -(-(1024 * 7168 * 2) // 256) * 256
+    assert out.value == 256 + counters + y
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("magic", ctypes.c_uint32), ("version", ctypes.c_uint32), ("mode", ctypes.c_uint32),
+                ("num_experts", ctypes.c_uint32), ("n", ctypes.c_uint32), ("k", ctypes.c_uint32),
+                ("group_size", ctypes.c_uint32), ("reserved", ctypes.c_uint32), ("bytes", ctypes.c_uint64)]
+
+
+def _desc(mode=1, e=4, n=256, k=128):
+    d = Desc(0x34413457, 1, mode, e, n, k, 32, 0, 0)
+    d.bytes = 256 + e * (n // 128) * (k // 64) * 4608
+    return d
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails its host-side checks
+
+
+def _masked(lib, d, flags=0, ws_bytes=256, k=128, expected_m=1):
+    return lib.moe_w4a16_masked(FAKE, ctypes.c_int(d.num_experts), 16, k, FAKE, expected_m, ctypes.byref(d), FAKE,
+                                None, 8, 2, None, ctypes.c_uint32(flags), FAKE, FAKE, ctypes.c_size_t(ws_bytes),
+                                None)
+
+
+def test_gemm_host_checks_reject_before_launch(lib):
+    d = _desc()
+    bad = _desc()
+    bad.magic = 0
+    assert _masked(lib, bad) == 3                     # not a prepared-weight descriptor
+    stale = _desc()
+    stale.version = 0
+    assert _masked(lib, stale) == 3                   # stale layout version
+    assert _masked(lib, d, flags=1) == 3              # SwiGLU needs a gate_up-mode weight
+    assert _masked(lib, _desc(mode=2), flags=2) == 3  # combine needs a plain weight
+    assert _masked(lib, d, flags=3) == 1              # SwiGLU and combine together
+    assert _masked(lib, d, flags=2) == 1              # combine without router weights
+    assert _masked(lib, d, k=64) == 1                 # K differs from the prepared weight
+    assert _masked(lib, d, ws_bytes=64) == 4          # workspace too small
+    assert _masked(lib, d, expected_m=0) == 1         # expected_m must be positive
+    g = _desc()
+    g.group_size = 64
+    assert _masked(lib, g) == 2
+
+
+def test_launch_counter_starts_at_zero_without_gpu(lib):
+    lib.moe_w4a16_launch_count.restype = ctypes.c_uint64
+    assert lib.moe_w4a16_launch_count() == 0

@@ -1,0 +1,233 @@
+"""GPU parity of the grouped GEMM entry points against the CPU oracle.
+
+Both kernel families (decode: warp MMA; prefill: tcgen05) x the three layouts
+x the epilogues, on small shapes that span several tiles and ragged tails,
+plus the edge cases of the method: empty experts, one expert holding every
+row, rows per expert around the 8/16/32/128/256 tile edges, poison in padding
+rows, and device-detected index errors.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_util import (assert_close, bits_to_dev, dev_to_bits, distinct_topk, i32_to_dev, ids_from_counts,
+                      prepare_dev, random_acts, random_weights)
+
+pytestmark = pytest.mark.gpu
+
+M = pytest.importorskip("w4a16_int4_mixture_grouped_gb300") if torch.cuda.is_available() else None
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+def _indexed_run(a_bits, qw, sc, ids, block_m, mode=1, flags=0, weights=None, a_per_row=False):
+    t, k = ids.shape
+    e = qw.shape[0]
+    pw = prepare_dev(qw, sc, mode, DEV)
+    f = flags | (M.FLAG_A_PER_ROW if a_per_row else 0)
+    ws = M.workspace(t, k, pw.n, f, DEV)
+    s_ids, e_ids, npp, _ = M.align(i32_to_dev(ids, DEV), e, block_m, ws)
+    w_dev = torch.from_numpy(weights).to(DEV) if weights is not None else None
+    out = M.indexed(bits_to_dev(a_bits, DEV), pw, s_ids, e_ids, npp, t, k, block_m, ws, flags=f, topk_weights=w_dev)
+    code = M.get_device_error(ws)
+    assert code == 0, f"device error {code}"
+    return dev_to_bits(out)
+
+
+@pytest.mark.parametrize("block_m", [8, 16, 32, 48, 128, 256])
+def test_indexed_plain_matches_oracle(block_m):
+    rng = np.random.default_rng(100 + block_m)
+    e, t, k, kd, n = 6, 70, 3, 320, 512
+    a = random_acts(rng, t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    ids = distinct_topk(rng, t, e, k)
+    ref = O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), n)
+    gpu = _indexed_run(a, qw, sc, ids, block_m)
+    assert_close(gpu, ref, f"indexed bm={block_m}")
+
+
+@pytest.mark.parametrize("block_m", [32, 256])
+@pytest.mark.parametrize("counts", [[1, 7, 8, 9, 0, 31, 32, 33], [127, 128, 129, 0, 255, 256, 257, 2], [600, 0, 0, 0]])
+def test_indexed_tile_edges(block_m, counts):
+    rng = np.random.default_rng(sum(counts) + block_m)
+    e, kd, n = len(counts), 128, 256
+    ids = ids_from_counts(rng, counts)
+    a = random_acts(rng, ids.shape[0], kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    ref = O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), n)
+    gpu = _indexed_run(a, qw, sc, ids, block_m)
+    assert_close(gpu, ref, f"edges bm={block_m}")
+
+
+@pytest.mark.parametrize("block_m", [32, 256])
+def test_indexed_gate_up_mode_and_swiglu(block_m):
+    rng = np.random.default_rng(7 + block_m)
+    e, t, k, kd, n = 5, 90, 2, 256, 512
+    a = random_acts(rng, t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    ids = distinct_topk(rng, t, e, k)
+    y = O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), n)
+    plain = _indexed_run(a, qw, sc, ids, block_m, mode=2)
+    assert_close(plain, y, "gate_up mode plain store")
+    h = _indexed_run(a, qw, sc, ids, block_m, mode=2, flags=M.FLAG_SWIGLU)
+    assert_close(h, O.swiglu(y), "fused SwiGLU")
+
+
+@pytest.mark.parametrize("block_m", [16, 32, 128, 256])
+def test_indexed_down_with_combine(block_m):
+    rng = np.random.default_rng(31 + block_m)
+    e, t, k, kd, n = 7, 40, 4, 192, 768
+    ids = distinct_topk(rng, t, e, k)
+    h = random_acts(rng, t * k, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    w = rng.uniform(0, 1, size=(t, k)).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)
+    y = O.indexed_gemm(h, ids, lambda x: (qw[x], sc[x]), n, a_per_routed_row=True)
+    ref = O.combine(y, w)
+    gpu = _indexed_run(h, qw, sc, ids, block_m, flags=M.FLAG_COMBINE, weights=w, a_per_row=True)
+    assert_close(gpu, ref, f"combine bm={block_m}")
+    # repeated call reuses the workspace counters
+    gpu2 = _indexed_run(h, qw, sc, ids, block_m, flags=M.FLAG_COMBINE, weights=w, a_per_row=True)
+    assert np.array_equal(gpu, gpu2)
+
+
+@pytest.mark.parametrize("kernel", ["decode", "prefill"])
+def test_contiguous_matches_oracle_and_ignores_poisoned_padding(kernel, monkeypatch):
+    monkeypatch.setenv("MOE_W4A16_FORCE_KERNEL", kernel)
+    rng = np.random.default_rng(41)
+    e, t, k, kd, n = 6, 150, 2, 256, 512
+    ids = distinct_topk(rng, t, e, k)
+    a = random_acts(rng, t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    row_ids, m_idx = O.contiguous_layout(ids, e)
+    a_pad = O.gather_rows(a, row_ids, k)
+    a_pad[row_ids < 0] = 0x7FC0                      # NaN in every padding row
+    pw = prepare_dev(qw, sc, 1, DEV)
+    ws = M.workspace(t, k, n, 0, DEV)
+    out = torch.full((a_pad.shape[0], n), 12345.0, dtype=torch.bfloat16, device=DEV)
+    M.contiguous(bits_to_dev(a_pad, DEV), i32_to_dev(m_idx, DEV), pw, ws, out=out)
+    assert M.get_device_error(ws) == 0
+    gpu = dev_to_bits(out)
+    ref, valid = O.contiguous_gemm(a_pad, m_idx, lambda x: (qw[x], sc[x]), n)
+    assert_close(gpu[valid], ref[valid], f"contiguous {kernel}")
+    sentinel = dev_to_bits(torch.full((1,), 12345.0, dtype=torch.bfloat16))[0]
+    assert np.all(gpu[~valid] == sentinel), "padding rows were written"
+
+
+@pytest.mark.parametrize("kernel", ["decode", "prefill"])
+@pytest.mark.parametrize("expected_m", [1, 40, 1000])
+def test_masked_matches_oracle_expected_m_only_picks_launch(kernel, expected_m, monkeypatch):
+    monkeypatch.setenv("MOE_W4A16_FORCE_KERNEL", kernel)
+    rng = np.random.default_rng(51)
+    e, t, k, kd, n, max_m = 9, 120, 3, 192, 256, 96
+    ids = distinct_topk(rng, t, e, k)
+    a = random_acts(rng, t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    masked_m, mrows = O.masked_layout(ids, e, max_m)
+    a3 = O.gather_rows(a, mrows.reshape(-1), k).reshape(e, max_m, kd)
+    for ex in range(e):
+        a3[ex, masked_m[ex]:] = 0x7FC0               # NaN past each count
+    pw = prepare_dev(qw, sc, 1, DEV)
+    ws = M.workspace(t, k, n, 0, DEV)
+    out = M.masked(bits_to_dev(a3, DEV), i32_to_dev(masked_m, DEV), expected_m, pw, ws)
+    assert M.get_device_error(ws) == 0
+    ref, valid = O.masked_gemm(a3, masked_m, lambda x: (qw[x], sc[x]), n)
+    assert_close(dev_to_bits(out)[valid], ref[valid], f"masked {kernel} em={expected_m}")
+
+
+@pytest.mark.parametrize("kernel", ["decode", "prefill"])
+def test_masked_swiglu_and_combine(kernel, monkeypatch):
+    monkeypatch.setenv("MOE_W4A16_FORCE_KERNEL", kernel)
+    rng = np.random.default_rng(61)
+    e, t, k, kd, n, max_m = 8, 64, 2, 128, 512, 40
+    ids = distinct_topk(rng, t, e, k)
+    a = random_acts(rng, t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    masked_m, mrows = O.masked_layout(ids, e, max_m)
+    a3 = O.gather_rows(a, mrows.reshape(-1), k).reshape(e, max_m, kd)
+    ws = M.workspace(t, k, n, M.FLAG_COMBINE, DEV)
+    y = O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), n)
+    # SwiGLU on a gate_up-mode weight
+    pw2 = prepare_dev(qw, sc, 2, DEV)
+    h = M.masked(bits_to_dev(a3, DEV), i32_to_dev(masked_m, DEV), 8, pw2, ws, flags=M.FLAG_SWIGLU)
+    valid = (mrows.reshape(-1) >= 0)
+    assert_close(dev_to_bits(h)[valid], O.swiglu(y)[mrows.reshape(-1)[valid]], f"masked swiglu {kernel}")
+    # combine on a plain weight
+    w = rng.uniform(0, 1, size=(t, k)).astype(np.float32)
+    pw1 = prepare_dev(qw, sc, 1, DEV)
+    out = M.masked(bits_to_dev(a3, DEV), i32_to_dev(masked_m, DEV), 8, pw1, ws, flags=M.FLAG_COMBINE,
+                   row_ids=i32_to_dev(mrows.reshape(-1), DEV), num_tokens=t, top_k=k,
+                   topk_weights=torch.from_numpy(w).to(DEV))
+    assert M.get_device_error(ws) == 0
+    assert_close(dev_to_bits(out), O.combine(y, w), f"masked combine {kernel}")
+
+
+def test_layout_equivalence_on_gpu():
+    """indexed, contiguous and masked give the same valid rows (same kernel family: bit-identical)."""
+    rng = np.random.default_rng(71)
+    e, t, k, kd, n = 8, 48, 2, 256, 256
+    ids = distinct_topk(rng, t, e, k)
+    a = random_acts(rng, t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    y_idx = _indexed_run(a, qw, sc, ids, 32)
+    pw = prepare_dev(qw, sc, 1, DEV)
+    ws = M.workspace(t, k, n, 0, DEV)
+    masked_m, mrows = O.masked_layout(ids, e, 32)
+    a3 = O.gather_rows(a, mrows.reshape(-1), k).reshape(e, 32, kd)
+    ym = dev_to_bits(M.masked(bits_to_dev(a3, DEV), i32_to_dev(masked_m, DEV), 1, pw, ws))
+    v = mrows.reshape(-1) >= 0
+    assert np.array_equal(ym[v], y_idx[mrows.reshape(-1)[v]])
+
+
+def test_empty_routing_is_a_no_op():
+    rng = np.random.default_rng(81)
+    qw, sc = random_weights(rng, 4, 256, 128)
+    pw = prepare_dev(qw, sc, 1, DEV)
+    ws = M.workspace(1, 1, 256, 0, DEV)
+    ids = torch.zeros((0, 2), dtype=torch.int32, device=DEV)
+    s_ids, e_ids, npp, _ = M.align(ids, 4, 32, ws)
+    a = torch.zeros((0, 128), dtype=torch.bfloat16, device=DEV)
+    out = M.indexed(a, pw, s_ids, e_ids, npp, 0, 2, 32, ws)
+    assert out.shape == (0, 256)
+    masked_m = torch.zeros(4, dtype=torch.int32, device=DEV)
+    a3 = torch.zeros((4, 16, 128), dtype=torch.bfloat16, device=DEV)
+    M.masked(a3, masked_m, 1, pw, ws)
+    assert M.get_device_error(ws) == 0
+
+
+def test_device_index_checks_do_not_fault():
+    rng = np.random.default_rng(91)
+    qw, sc = random_weights(rng, 4, 256, 128)
+    pw = prepare_dev(qw, sc, 1, DEV)
+    ws = M.workspace(8, 1, 256, 0, DEV)
+    a = bits_to_dev(random_acts(rng, 8, 128), DEV)
+    # masked_m above the budget -> capacity error, no out-of-bounds access
+    a3 = torch.zeros((4, 16, 128), dtype=torch.bfloat16, device=DEV)
+    M.masked(a3, i32_to_dev(np.array([3, 40, 0, 1]), DEV), 4, pw, ws)
+    assert M.get_device_error(ws) == 5
+    M.clear_device_error(ws)
+    # sorted_ids holding an id past the sentinel and an expert id out of range
+    s_ids = i32_to_dev(np.array([0, 1, 99, 8] + [8] * 28), DEV)
+    e_ids = i32_to_dev(np.array([7]), DEV)
+    npp = i32_to_dev(np.array([32]), DEV)
+    M.indexed(a, pw, s_ids, e_ids, npp, 8, 1, 32, ws)
+    assert M.get_device_error(ws) == 8
+    M.clear_device_error(ws)
+    e_ids = i32_to_dev(np.array([1]), DEV)
+    M.indexed(a, pw, s_ids, e_ids, npp, 8, 1, 32, ws)
+    assert M.get_device_error(ws) == 8
+
+
+def test_mode_mismatch_fails_before_launch():
+    rng = np.random.default_rng(92)
+    qw, sc = random_weights(rng, 2, 256, 64)
+    pw = prepare_dev(qw, sc, 1, DEV)
+    ws = M.workspace(4, 1, 256, 0, DEV)
+    a3 = torch.zeros((2, 4, 64), dtype=torch.bfloat16, device=DEV)
+    mm = torch.zeros(2, dtype=torch.int32, device=DEV)
+    before = M.launch_count()
+    with pytest.raises(M.MoeW4A16Error) as ei:
+        M.masked(a3, mm, 1, pw, ws, flags=M.FLAG_SWIGLU)
+    assert ei.value.name == "ERR_MODE_MISMATCH"
+    assert M.launch_count() == before

@@ -1,0 +1,300 @@
+// Decode-regime grouped GEMM: few routed rows per expert.
+//
+// The Chord page (section "H200 and Blackwell indexed decode") observes that
+// at a few rows per expert the wide tensor-core path is barrier-bound, and
+// swaps the MMA operands so the dequantised weights fill the MMA M dimension
+// with m16n8k16 tiles and a small block-M. This kernel keeps that idea on
+// sm_103a: the weight stream is the whole cost, so
+//   * one producer warp streams each work unit's prepared chunks (4.5 KB each)
+//     and the block's activation rows (128 B per row per k-chunk) into a
+//     6-stage shared-memory ring with 1-D bulk async copies (16-B aligned,
+//     complete_tx on an mbarrier, weights marked evict-first in L2);
+//   * eight consumer warps each own 16 channels of both 128-channel chunks of
+//     the unit: a lane's 16-byte load yields four k-steps of A operands, which
+//     are dequantised in registers (dequant_fu: (q - 8) * s, one BF16 rounding)
+//     and fed to mma.m16n8k16 against up to four 8-row token tiles;
+//   * the stage is released as soon as its bytes are in registers.
+// Work units are (row block <= 32 rows, 256-channel group), assigned to a
+// persistent grid in a fixed interleaved order once the device-side block
+// count is known (a semi-static schedule, the page's 186 us vs 216 us point).
+// Epilogues: BF16 store, SwiGLU (gate and up channels of a unit sit in the
+// same lane), or the top-k combine (routed rows staged in BF16, the last of
+// the top_k arrivals for a (token, channel slice) sums them in slot order).
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "rows.cuh"
+
+namespace moe {
+namespace decode {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kRows = kDecodeRows;                      // 32
+constexpr int kActStride = 144;                         // 128 B of k + 16 B pad (conflict-free ldmatrix)
+constexpr int kActBytes = kRows * kActStride;           // 4608
+constexpr int kStageBytes = 2 * kChunkBytes + kActBytes;  // 13824
+constexpr int kStages = 6;
+constexpr int kBarOffset = kStages * kStageBytes;
+constexpr int kMiscBytes = 256;
+constexpr int kSlices = kConsumerWarps;                 // combine counter slices per group
+
+__host__ __device__ constexpr int smem_bytes(int prefix_entries) {
+  return kBarOffset + kMiscBytes + prefix_entries * 4;
+}
+
+struct Smem {
+  uint32_t stages;  // shared address of stage 0
+  uint32_t full;    // shared address of full[0]
+  uint32_t empty;   // shared address of empty[0]
+  volatile int* abort_flag;
+  int* prefix;
+};
+
+__device__ __forceinline__ void store_bf16(uint16_t* base, int64_t idx, float v) {
+  base[idx] = f32_to_bf16_rn(v);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Smem s;
+  s.stages = smem_u32(smem);
+  s.full = smem_u32(smem + kBarOffset);
+  s.empty = s.full + kStages * 8;
+  s.abort_flag = reinterpret_cast<volatile int*>(smem + kBarOffset + 2 * kStages * 8);
+  s.prefix = reinterpret_cast<int*>(smem + kBarOffset + kMiscBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(s.full + 8 * i, 1);
+      mbar_init(s.empty + 8 * i, kConsumerWarps);
+    }
+    *s.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (p.layout == MOE_W4A16_LAYOUT_MASKED && warp == 0) masked_prefix_warp(p, kRows, s.prefix);
+  __syncthreads();
+
+  const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED ? p.block_m : kRows;
+  const int nblk = num_row_blocks(p, rows_per_block, s.prefix);
+  const int64_t total_units = static_cast<int64_t>(nblk) * p.NG;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool issued_any = false;
+    for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
+      int local;
+      const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
+      if (e < 0) continue;
+      const RowRef rr = block_row(p, blk, e, local, rows_per_block, lane);
+      const bool valid = rr.a_row >= 0;
+      const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+      if (vmask == 0) continue;
+      const uint32_t tx = 2u * kChunkBytes + 128u * __popc(vmask);
+      const uint8_t* c0 = p.chunks + (static_cast<size_t>(e) * p.NB + 2 * gp) * p.KC * kChunkBytes;
+      const uint8_t* c1 = c0 + static_cast<size_t>(p.KC) * kChunkBytes;
+      const uint16_t* arow = p.a + static_cast<int64_t>(valid ? rr.a_row : 0) * p.K;
+      for (int kc = 0; kc < p.KC; ++kc) {
+        if (!warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err)) goto producer_done;
+        const uint32_t full = s.full + 8 * stage;
+        if (lane == 0) mbar_arrive_expect_tx(full, tx);
+        __syncwarp();
+        const uint32_t sb = s.stages + stage * kStageBytes;
+        if (lane == 0) bulk_g2s_hint(sb, c0 + static_cast<size_t>(kc) * kChunkBytes, kChunkBytes, full, pol);
+        if (lane == 1)
+          bulk_g2s_hint(sb + kChunkBytes, c1 + static_cast<size_t>(kc) * kChunkBytes, kChunkBytes, full, pol);
+        if (valid) bulk_g2s(sb + 2 * kChunkBytes + lane * kActStride, arow + kc * kChunkK, 128, full);
+        issued_any = true;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  producer_done:
+    if (*s.abort_flag && issued_any) {
+      // let copies already in flight land before the CTA's shared memory is released
+      for (int i = 0; i < kStages; ++i) {
+        int st = stage - 1 - i;
+        uint32_t ph = phase;
+        if (st < 0) {
+          st += kStages;
+          ph ^= 1u;
+        }
+        mbar_drain(s.full + 8 * st, ph);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int g = lane >> 2, t = lane & 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    const uint32_t wq_off = (warp * 32 + lane) * 16;
+    const uint32_t sc_off = kChunkWBytes + (warp * 8 + g) * 8;
+    for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
+      int local;
+      const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
+      if (e < 0) continue;
+      const RowRef rr = block_row(p, blk, e, local, rows_per_block, lane);
+      const unsigned vmask = __ballot_sync(0xffffffffu, rr.a_row >= 0);
+      if (vmask == 0) continue;
+      const int ntiles = (32 - __clz(vmask) + 7) >> 3;
+
+      float acc[2][4][4];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
+
+      for (int kc = 0; kc < p.KC; ++kc) {
+        if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) goto consumer_done;
+        const uint32_t sb = s.stages + stage * kStageBytes;
+        const uint4 wq0 = lds128(sb + wq_off);
+        const uint4 wq1 = lds128(sb + kChunkBytes + wq_off);
+        const uint2 sc0 = lds64(sb + sc_off);
+        const uint2 sc1 = lds64(sb + kChunkBytes + sc_off);
+        uint32_t b[4][4][2];
+        const uint32_t act = sb + 2 * kChunkBytes + (lane & 7) * kActStride + (lane >> 3) * 16;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          if (nt < ntiles) {
+            ldsm_x4(act + nt * 8 * kActStride, b[nt][0][0], b[nt][0][1], b[nt][1][0], b[nt][1][1]);
+            ldsm_x4(act + nt * 8 * kActStride + 64, b[nt][2][0], b[nt][2][1], b[nt][3][0], b[nt][3][1]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s.empty + 8 * stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        const uint32_t w0[4] = {wq0.x, wq0.y, wq0.z, wq0.w};
+        const uint32_t w1[4] = {wq1.x, wq1.y, wq1.z, wq1.w};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          uint32_t sg, sg8, a[4];
+          scale_pairs(sc0, ks >> 1, sg, sg8);
+          dequant_fu(w0[ks], sg, sg8, a);
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt)
+            if (nt < ntiles) mma_16816(acc[0][nt], a, b[nt][ks][0], b[nt][ks][1]);
+          scale_pairs(sc1, ks >> 1, sg, sg8);
+          dequant_fu(w1[ks], sg, sg8, a);
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt)
+            if (nt < ntiles) mma_16816(acc[1][nt], a, b[nt][ks][0], b[nt][ks][1]);
+        }
+      }
+
+      // ---------------------------------------------------------- epilogue
+      // acc[c][nt]: channels ch = c*128 + warp*16 + g (+8), token slots nt*8 + 2t (+1)
+      {
+        const bool swiglu = p.flags & MOE_W4A16_FLAG_SWIGLU;
+        const bool combine = p.flags & MOE_W4A16_FLAG_COMBINE;
+        const int chl = warp * 16 + g;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          if (nt >= ntiles) break;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int slot = nt * 8 + 2 * t + j;
+            const int out_row = __shfl_sync(0xffffffffu, combine ? rr.flat : rr.out_row, slot);
+            const int a_ok = __shfl_sync(0xffffffffu, rr.a_row, slot);
+            if (a_ok < 0 || out_row < 0) continue;
+            const float v00 = acc[0][nt][j], v08 = acc[0][nt][2 + j];
+            const float v10 = acc[1][nt][j], v18 = acc[1][nt][2 + j];
+            if (swiglu) {
+              uint16_t* dst = p.c + static_cast<int64_t>(out_row) * p.c_cols + gp * kChunkN;
+              store_bf16(dst, chl, silu_f32(round_to_bf16(v00)) * round_to_bf16(v10));
+              store_bf16(dst, chl + 8, silu_f32(round_to_bf16(v08)) * round_to_bf16(v18));
+            } else {
+              uint16_t* base = combine ? p.y_ws : p.c;
+              const int64_t ld = combine ? p.N : p.c_cols;
+              uint16_t* dst0;
+              uint16_t* dst1;
+              if (p.mode == MOE_W4A16_MODE_GATE_UP) {
+                dst0 = base + static_cast<int64_t>(out_row) * ld + gp * kChunkN;
+                dst1 = base + static_cast<int64_t>(out_row) * ld + p.N / 2 + gp * kChunkN;
+              } else {
+                dst0 = base + static_cast<int64_t>(out_row) * ld + gp * kGroupN;
+                dst1 = dst0 + kChunkN;
+              }
+              store_bf16(dst0, chl, v00);
+              store_bf16(dst0, chl + 8, v08);
+              store_bf16(dst1, chl, v10);
+              store_bf16(dst1, chl + 8, v18);
+            }
+          }
+        }
+        if (combine) {
+          // this warp's 32 channels of every valid row are staged; the last of the
+          // top_k arrivals for (token, group, warp slice) sums the slots in order
+          __threadfence();
+          __syncwarp();
+          int tok = -1;
+          bool last = false;
+          if (rr.a_row >= 0 && rr.flat >= 0) {
+            tok = rr.flat / p.top_k;
+            last = atomicAdd(combine_counter(p, tok, gp, warp, kSlices), 1) == p.top_k - 1;
+          }
+          unsigned lm = __ballot_sync(0xffffffffu, last);
+          if (lm) __threadfence();
+          const int ch = (lane < 16 ? 0 : kChunkN) + warp * 16 + (lane & 15);
+          while (lm) {
+            const int src = __ffs(lm) - 1;
+            lm &= lm - 1u;
+            const int tt = __shfl_sync(0xffffffffu, tok, src);
+            float sum = 0.f;
+            for (int j = 0; j < p.top_k; ++j) {
+              const float w = p.topk_weights[static_cast<int64_t>(tt) * p.top_k + j];
+              const uint16_t y = __ldcg(p.y_ws + (static_cast<int64_t>(tt) * p.top_k + j) * p.N + gp * kGroupN + ch);
+              sum += w * bf16_to_f32(y);
+            }
+            p.c[static_cast<int64_t>(tt) * p.N + gp * kGroupN + ch] = f32_to_bf16_rn(sum);
+          }
+        }
+      }
+    }
+  consumer_done:;
+  }
+}
+
+}  // namespace decode
+
+cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
+  using namespace decode;
+  const DeviceInfo& di = device_info(device);
+  const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
+  const int smem = smem_bytes(prefix_entries);
+  static bool attr_set[64] = {false};
+  if (device >= 0 && device < 64 && !attr_set[device]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
+    if (e != cudaSuccess) return e;
+    attr_set[device] = true;
+  }
+  // upper bound of work units known on the host
+  int64_t max_blocks;
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED) max_blocks = p.sorted_cap / p.block_m;
+  else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) max_blocks = p.m_pad / kRows;
+  else max_blocks = static_cast<int64_t>(p.num_experts) * ((p.max_m + kRows - 1) / kRows);
+  int64_t units = max_blocks * p.NG;
+  int64_t grid = static_cast<int64_t>(di.sm_count) * 2;
+  if (units < grid) grid = units;
+  if (grid < 1) grid = 1;
+  decode_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p);
+  note_launch();
+  if (grid_out) *grid_out = static_cast<int>(grid);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

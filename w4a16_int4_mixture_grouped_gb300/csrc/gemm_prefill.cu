@@ -1,0 +1,484 @@
+// Prefill-regime grouped GEMM: many routed rows per expert, tcgen05 tensor cores.
+//
+// The Chord page's grouped kernels (section "Grouped SM90 kernels") are
+// persistent and warp-specialised: a producer stages activations, packed
+// weights and scale tiles with TMA while consumers run the tensor-core MMA
+// and write BF16. On sm_103a the MMA is tcgen05 with its accumulator in
+// tensor memory (TMEM), issued by one thread, so the roles become:
+//
+//   warp 0      : allocates TMEM; lane 0 streams the unit's two prepared
+//                 chunks per k-chunk (9 KB) with 1-D bulk copies
+//   warp 1      : lane 0 issues tcgen05.mma (M = 128 channels per tile, two
+//                 tiles per unit, N = the block's rows rounded up to 16, K = 16)
+//   warps 2-3   : gather the block's activation rows (cp.async, 16 B each) into
+//                 a 128-byte-swizzled K-major tile: rows 0-127 / 128-255
+//   warps 4-11  : dequantise (warps 4-7: channel tile 0, warps 8-11: tile 1)
+//                 into a 128-byte-swizzled K-major BF16 tile with stmatrix,
+//                 then run the epilogue from TMEM
+//
+// Operands are "swapped" as in the page's decode design: the dequantised
+// weights are the MMA's M operand and the routed rows its N operand, so a
+// block of r rows costs ceil(r/16)*16 columns, not a 128-row tile. Both
+// accumulators (2 x 256 columns of FP32) live in TMEM; for SwiGLU the gate
+// and up tiles of a unit hold matching channels in the same TMEM lane.
+// Every mbarrier wait is bounded (common.cuh); no named barrier is used after
+// the role split, so an abort can never strand a warp.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "rows.cuh"
+
+namespace moe {
+namespace prefill {
+
+constexpr int kThreads = 384;
+constexpr int kRows = kPrefillRows;        // 256
+constexpr int kXStages = 3;
+constexpr int kWStages = 2;
+constexpr int kPStages = 4;
+constexpr int kXBytes = kRows * 128;       // 32 KB: 256 rows x 64 k x bf16
+constexpr int kWTileBytes = kChunkN * 128; // 16 KB: 128 channels x 64 k x bf16
+constexpr int kWBytes = 2 * kWTileBytes;   // 32 KB
+constexpr int kPBytes = 2 * kChunkBytes;   // 9 KB
+constexpr int kXOff = 0;
+constexpr int kWOff = kXOff + kXStages * kXBytes;
+constexpr int kPOff = kWOff + kWStages * kWBytes;
+constexpr int kBarOff = kPOff + kPStages * kPBytes;
+constexpr int kNumBars = 2 * kPStages + 2 * kXStages + 2 * kWStages + 3;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kXRowOff = kMiscOff + 16;             // int [2][128] producer row tables
+constexpr int kPrefixOff = kXRowOff + 2 * 128 * 4;
+constexpr int kTmemCols = 512;
+constexpr int kSlices = 4;                          // combine counter slices per group
+
+__host__ __device__ constexpr int smem_bytes(int prefix_entries) {
+  return kPrefixOff + prefix_entries * 4 + 1024;  // + alignment slack
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, int ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, int ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// K-major operand with 128-byte swizzle: rows of 128 B, 8-row atoms of 1024 B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused for this swizzle)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset: 8 rows x 128 B
+  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+  return d;
+}
+// kind::f16 instruction descriptor: FP32 accumulate, BF16 A and B, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Highest valid row of a block + 1 (warp-uniform), rows scanned by a full warp.
+__device__ __forceinline__ int block_extent(const GemmParams& p, int blk, int e, int local, int rows) {
+  const int lane = threadIdx.x & 31;
+  int hi = 0;
+  for (int i = lane; i < rows; i += 32) {
+    const RowRef r = block_row(p, blk, e, local, rows, i);
+    if (r.a_row >= 0) hi = i + 1;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  return hi;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled operand tiles
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + kBarOff;
+  const uint32_t p_full = bar0, p_empty = p_full + 8 * kPStages;
+  const uint32_t x_full = p_empty + 8 * kPStages, x_empty = x_full + 8 * kXStages;
+  const uint32_t w_full = x_empty + 8 * kXStages, w_empty = w_full + 8 * kWStages;
+  const uint32_t acc_full = w_empty + 8 * kWStages, acc_empty = acc_full + 8, drain_bar = acc_empty + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+  int* xrow_tab = reinterpret_cast<int*>(smem + kXRowOff);
+  int* prefix = reinterpret_cast<int*>(smem + kPrefixOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPStages; ++i) {
+      mbar_init(p_full + 8 * i, 1);
+      mbar_init(p_empty + 8 * i, 8);
+    }
+    for (int i = 0; i < kXStages; ++i) {
+      mbar_init(x_full + 8 * i, 64);
+      mbar_init(x_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(w_full + 8 * i, 8);
+      mbar_init(w_empty + 8 * i, 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 8);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (p.layout == MOE_W4A16_LAYOUT_MASKED && warp == 1) masked_prefix_warp(p, kRows, prefix);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED    ? p.block_m
+                             : p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS ? kContigSeg
+                                                                        : kRows;
+  const int nblk = num_row_blocks(p, rows_per_block, prefix);
+  const int64_t total_units = static_cast<int64_t>(nblk) * p.NG;
+
+  if (warp == 0) {
+    // ----------------------------------------------------- packed weights
+    const uint64_t pol = policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool issued = false;
+    for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
+      int local;
+      const int e = block_expert(p, blk, rows_per_block, prefix, local);
+      if (e < 0) continue;
+      if (block_extent(p, blk, e, local, rows_per_block) == 0) continue;
+      const uint8_t* c0 = p.chunks + (static_cast<size_t>(e) * p.NB + 2 * gp) * p.KC * kChunkBytes;
+      const uint8_t* c1 = c0 + static_cast<size_t>(p.KC) * kChunkBytes;
+      for (int kc = 0; kc < p.KC; ++kc) {
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(p_empty + 8 * stage, phase ^ 1u, abort_flag, p.err);
+          if (ok) {
+            const uint32_t full = p_full + 8 * stage;
+            const uint32_t dst = sbase + kPOff + stage * kPBytes;
+            mbar_arrive_expect_tx(full, kPBytes);
+            bulk_g2s_hint(dst, c0 + static_cast<size_t>(kc) * kChunkBytes, kChunkBytes, full, pol);
+            bulk_g2s_hint(dst + kChunkBytes, c1 + static_cast<size_t>(kc) * kChunkBytes, kChunkBytes, full, pol);
+            issued = true;
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) goto p_done;
+        if (++stage == kPStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  p_done:
+    if (lane == 0 && *abort_flag && issued) {
+      for (int i = 0; i < kPStages; ++i) {
+        int st = stage - 1 - i;
+        uint32_t ph = phase;
+        if (st < 0) {
+          st += kPStages;
+          ph ^= 1u;
+        }
+        mbar_drain(p_full + 8 * st, ph);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------- MMA issuer
+    int xs = 0, ws = 0;
+    uint32_t xph = 0, wph = 0, aph = 0;
+    for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const int blk = static_cast<int>(u / p.NG);
+      int local;
+      const int e = block_expert(p, blk, rows_per_block, prefix, local);
+      if (e < 0) continue;
+      const int ext = block_extent(p, blk, e, local, rows_per_block);
+      if (ext == 0) continue;
+      const int nr = (ext + 15) & ~15;
+      const uint32_t idesc = idesc_bf16(128, nr);
+      if (lane == 0) {
+        bool ok = mbar_wait(acc_empty, aph ^ 1u, abort_flag, p.err);
+        tc_fence_after();
+        for (int kc = 0; ok && kc < p.KC; ++kc) {
+          ok = mbar_wait(x_full + 8 * xs, xph, abort_flag, p.err) && mbar_wait(w_full + 8 * ws, wph, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t xa = sbase + kXOff + xs * kXBytes;
+          const uint32_t wa = sbase + kWOff + ws * kWBytes;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bdesc = sw128_desc(xa + ks * 32);
+            const uint32_t acc = (kc | ks) != 0;
+            tc_mma(tmem, sw128_desc(wa + ks * 32), bdesc, idesc, acc);
+            tc_mma(tmem + 256, sw128_desc(wa + kWTileBytes + ks * 32), bdesc, idesc, acc);
+          }
+          tc_commit(x_empty + 8 * xs);
+          tc_commit(w_empty + 8 * ws);
+          if (++xs == kXStages) {
+            xs = 0;
+            xph ^= 1u;
+          }
+          if (++ws == kWStages) {
+            ws = 0;
+            wph ^= 1u;
+          }
+        }
+        if (ok) tc_commit(acc_full);
+      }
+      __syncwarp();
+      aph ^= 1u;
+      if (warp_aborted(abort_flag)) break;
+    }
+    if (lane == 0) {
+      // every MMA issued by this thread completes before TMEM is released
+      tc_commit(drain_bar);
+      mbar_drain(drain_bar, 0);
+    }
+  } else if (warp < 4) {
+    // ----------------------------------------------------- activation rows
+    const int xw = warp - 2;                 // rows [128*xw, 128*xw + 128)
+    int* xrow = xrow_tab + xw * 128;
+    int stage = 0, prev = -1;
+    uint32_t phase = 0;
+    for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const int blk = static_cast<int>(u / p.NG);
+      int local;
+      const int e = block_expert(p, blk, rows_per_block, prefix, local);
+      if (e < 0) continue;
+      const int ext = block_extent(p, blk, e, local, rows_per_block);
+      if (ext == 0) continue;
+      const int nr = (ext + 15) & ~15;
+      __syncwarp();
+      for (int m = 0; m < 4; ++m) {
+        const int i = xw * 128 + lane + 32 * m;
+        xrow[lane + 32 * m] = (i < nr) ? block_row(p, blk, e, local, rows_per_block, i).a_row : -1;
+      }
+      __syncwarp();
+      const int my_rows = min(128, max(0, nr - xw * 128));
+      for (int kc = 0; kc < p.KC; ++kc) {
+        if (!warp_wait(x_empty + 8 * stage, phase ^ 1u, abort_flag, p.err)) goto x_done;
+        const uint32_t xa = sbase + kXOff + stage * kXBytes;
+        for (int idx = lane; idx < my_rows * 8; idx += 32) {
+          const int jl = idx >> 3, c = idx & 7;
+          const int j = xw * 128 + jl;
+          const int ar = xrow[jl];
+          const uint16_t* src = p.a + static_cast<int64_t>(ar < 0 ? 0 : ar) * p.K + kc * kChunkK + c * 8;
+          cp_async16(xa + j * 128 + ((c ^ (j & 7)) << 4), src, ar < 0 ? 0u : 16u);
+        }
+        cp_async_commit();
+        if (prev >= 0) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(x_full + 8 * prev);
+        }
+        prev = stage;
+        if (++stage == kXStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  x_done:
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (prev >= 0 && !*abort_flag) mbar_arrive(x_full + 8 * prev);
+  } else {
+    // ----------------------------------------------------- dequant + epilogue
+    const int dw = warp - 4;            // 0..7
+    const int tile = dw >> 2;           // channel tile (chunk) of the unit
+    const int wq = dw & 3;              // m-tiles 2wq, 2wq+1 of the tile; TMEM lane quarter
+    const int g = lane >> 2;
+    int ps = 0, ws = 0;
+    uint32_t pph = 0, wph = 0, aph = 0;
+    const bool swiglu = p.flags & MOE_W4A16_FLAG_SWIGLU;
+    const bool combine = p.flags & MOE_W4A16_FLAG_COMBINE;
+    for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
+      int local;
+      const int e = block_expert(p, blk, rows_per_block, prefix, local);
+      if (e < 0) continue;
+      const int ext = block_extent(p, blk, e, local, rows_per_block);
+      if (ext == 0) continue;
+      const int nr = (ext + 15) & ~15;
+      for (int kc = 0; kc < p.KC; ++kc) {
+        if (!warp_wait(p_full + 8 * ps, pph, abort_flag, p.err)) goto d_done;
+        const uint32_t pa = sbase + kPOff + ps * kPBytes + tile * kChunkBytes;
+        uint4 wv[2];
+        uint2 sv[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          wv[j] = lds128(pa + ((2 * wq + j) * 32 + lane) * 16);
+          sv[j] = lds64(pa + kChunkWBytes + ((2 * wq + j) * 8 + g) * 8);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_empty + 8 * ps);
+        if (++ps == kPStages) {
+          ps = 0;
+          pph ^= 1u;
+        }
+        if (!warp_wait(w_empty + 8 * ws, wph ^ 1u, abort_flag, p.err)) goto d_done;
+        const uint32_t wt = sbase + kWOff + ws * kWBytes + tile * kWTileBytes;
+        const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t w4[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+          const int n = (2 * wq + j) * 16 + (mi & 1) * 8 + r8;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            uint32_t sg, sg8, a[4];
+            scale_pairs(sv[j], ks >> 1, sg, sg8);
+            dequant_fu(w4[ks], sg, sg8, a);
+            const int c = 2 * ks + (mi >> 1);
+            stsm_x4(wt + n * 128 + ((c ^ r8) << 4), a[0], a[1], a[2], a[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(w_full + 8 * ws);
+        if (++ws == kWStages) {
+          ws = 0;
+          wph ^= 1u;
+        }
+      }
+
+      // ------------------------------------------------- epilogue
+      if (!warp_wait(acc_full, aph, abort_flag, p.err)) goto d_done;
+      aph ^= 1u;
+      tc_fence_after();
+      {
+        const int q = wq;  // TMEM lanes 32q..32q+31 = channels 32q+lane of each tile
+        const int nchunks = nr >> 4;
+        for (int cc = tile; cc < nchunks; cc += 2) {
+          uint32_t d0[16], d1[16];
+          const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + cc * 16;
+          tmem_ld16(taddr, d0);
+          tmem_ld16(taddr + 256, d1);
+          tmem_wait_ld();
+          RowRef rr{-1, -1, -1};
+          if (lane < 16 && cc * 16 + lane < ext) rr = block_row(p, blk, e, local, rows_per_block, cc * 16 + lane);
+          const int chan = 32 * q + lane;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int a_ok = __shfl_sync(0xffffffffu, rr.a_row, j);
+            const int orow = __shfl_sync(0xffffffffu, combine ? rr.flat : rr.out_row, j);
+            if (a_ok < 0 || orow < 0) continue;
+            const float v0 = __uint_as_float(d0[j]), v1 = __uint_as_float(d1[j]);
+            if (swiglu) {
+              p.c[static_cast<int64_t>(orow) * p.c_cols + gp * kChunkN + chan] =
+                  f32_to_bf16_rn(silu_f32(round_to_bf16(v0)) * round_to_bf16(v1));
+            } else {
+              uint16_t* base = combine ? p.y_ws : p.c;
+              const int64_t ld = combine ? p.N : p.c_cols;
+              uint16_t* row = base + static_cast<int64_t>(orow) * ld;
+              if (p.mode == MOE_W4A16_MODE_GATE_UP) {
+                row[gp * kChunkN + chan] = f32_to_bf16_rn(v0);
+                row[p.N / 2 + gp * kChunkN + chan] = f32_to_bf16_rn(v1);
+              } else {
+                row[gp * kGroupN + chan] = f32_to_bf16_rn(v0);
+                row[gp * kGroupN + kChunkN + chan] = f32_to_bf16_rn(v1);
+              }
+            }
+          }
+          if (combine) {
+            __threadfence();
+            __syncwarp();
+            int tok = -1;
+            bool last = false;
+            if (rr.a_row >= 0 && rr.flat >= 0) {
+              tok = rr.flat / p.top_k;
+              last = atomicAdd(combine_counter(p, tok, gp, q, kSlices), 1) == p.top_k - 1;
+            }
+            unsigned lm = __ballot_sync(0xffffffffu, last);
+            if (lm) __threadfence();
+            while (lm) {
+              const int src = __ffs(lm) - 1;
+              lm &= lm - 1u;
+              const int tt = __shfl_sync(0xffffffffu, tok, src);
+              float s0 = 0.f, s1 = 0.f;
+              for (int j = 0; j < p.top_k; ++j) {
+                const float w = p.topk_weights[static_cast<int64_t>(tt) * p.top_k + j];
+                const uint16_t* yr = p.y_ws + (static_cast<int64_t>(tt) * p.top_k + j) * p.N + gp * kGroupN;
+                s0 += w * bf16_to_f32(__ldcg(yr + chan));
+                s1 += w * bf16_to_f32(__ldcg(yr + kChunkN + chan));
+              }
+              uint16_t* orow_p = p.c + static_cast<int64_t>(tt) * p.N + gp * kGroupN;
+              orow_p[chan] = f32_to_bf16_rn(s0);
+              orow_p[kChunkN + chan] = f32_to_bf16_rn(s1);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+  d_done:;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace prefill
+
+cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
+  using namespace prefill;
+  const DeviceInfo& di = device_info(device);
+  const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
+  const int smem = smem_bytes(prefix_entries);
+  static bool attr_set[64] = {false};
+  if (device >= 0 && device < 64 && !attr_set[device]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
+    if (e != cudaSuccess) return e;
+    attr_set[device] = true;
+  }
+  int64_t max_blocks;
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED) max_blocks = p.sorted_cap / p.block_m;
+  else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) max_blocks = p.m_pad / kContigSeg;
+  else max_blocks = static_cast<int64_t>(p.num_experts) * ((p.max_m + kRows - 1) / kRows);
+  int64_t units = max_blocks * p.NG;
+  int64_t grid = di.sm_count;
+  if (units < grid) grid = units;
+  if (grid < 1) grid = 1;
+  prefill_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p);
+  note_launch();
+  if (grid_out) *grid_out = static_cast<int>(grid);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,100 @@
+// Internal host/device declarations of the W4A16 MoE library (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe_w4a16.h"
+
+namespace moe {
+
+// Prepared-weight geometry (see prepare.cu for the full layout)
+constexpr int kChunkN = 128;           // output channels per chunk
+constexpr int kChunkK = 64;            // k per chunk
+constexpr int kChunkWBytes = 4096;     // 128 x 64 nibbles
+constexpr int kChunkSBytes = 512;      // 128 x 2 groups x bf16
+constexpr int kChunkBytes = kChunkWBytes + kChunkSBytes;  // 4608
+constexpr int kHeaderBytes = 256;      // prepared-buffer header
+constexpr int kGroupN = 2 * kChunkN;   // channels per GEMM work unit
+
+
+// Counts a kernel launch (moe_w4a16_launch_count).
+void note_launch(int n = 1);
+
+// Device properties memoised per device.
+struct DeviceInfo {
+  int sm_count = 0;
+  int max_smem_optin = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+const DeviceInfo& device_info(int device);
+
+// Work description of one grouped-GEMM call, shared by both kernel families.
+struct GemmParams {
+  const uint16_t* a;         // bf16 rows of length K
+  int64_t a_rows;            // rows of `a` (bounds check)
+  int K, N;                  // GEMM shape per expert
+  int KC;                    // K / 64
+  int NB;                    // N / 128 prepared channel blocks
+  int NG;                    // N / 256 work-unit channel groups
+  const uint8_t* chunks;     // first chunk of the prepared buffer
+  int num_experts;
+  uint32_t mode;             // MOE_W4A16_MODE_*
+  uint32_t flags;            // MOE_W4A16_FLAG_*
+  int layout;                // MOE_W4A16_LAYOUT_*
+
+  // indexed
+  const int32_t* sorted_ids;
+  const int32_t* expert_ids;
+  const int32_t* num_post_padded;
+  int block_m;
+  int64_t sorted_cap;        // entries of sorted_ids
+  int R;                     // routed rows = sentinel value
+  int a_div;                 // A row = flat id / a_div
+
+  // contiguous
+  const int32_t* m_indices;
+  int m_pad;
+
+  // masked
+  const int32_t* masked_m;
+  int max_m;
+
+  // combine
+  const int32_t* row_ids;    // contiguous / masked: flat id of a layout row
+  const float* topk_weights;
+  int num_tokens, top_k;
+  uint16_t* y_ws;            // bf16 [R, N] staging
+  int* counters;             // [num_tokens, NG]
+
+  // output
+  uint16_t* c;
+  int64_t c_rows;            // rows of c (bounds)
+  int c_cols;                // row length of c (N, or N/2 with SWIGLU)
+  int* err;                  // device error word
+};
+
+cudaError_t launch_prepare(const int32_t* qweight, const uint16_t* scales, int E, int N, int K, int mode,
+                           uint8_t* prepared, cudaStream_t stream);
+cudaError_t launch_dequant_check(const uint8_t* prepared, int E, int N, int K, int mode, int expert, uint16_t* out,
+                                 cudaStream_t stream);
+cudaError_t launch_align(const int32_t* topk_ids, int R, int E, int block_m, int max_m, int32_t* sorted_ids,
+                         int32_t* expert_ids, int32_t* num_post_padded, int32_t* counts, int32_t* masked_rows,
+                         int* err, cudaStream_t stream);
+cudaError_t launch_contiguous_layout(const int32_t* sorted_ids, const int32_t* expert_ids,
+                                     const int32_t* num_post_padded, int R, int m_pad, int32_t* m_indices,
+                                     int32_t* row_ids, cudaStream_t stream);
+cudaError_t launch_gather_rows(const uint16_t* src, int src_rows, int K, const int32_t* row_ids, int num_rows,
+                               int row_div, uint16_t* dst, int* err, cudaStream_t stream);
+
+// Returns the number of CTAs launched through *grid_out.
+cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out);
+cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out);
+
+// Rows per block the kernels use for the contiguous / masked layouts.
+constexpr int kDecodeRows = 32;
+constexpr int kPrefillRows = 256;
+constexpr int kContigSeg = 128;
+
+}  // namespace moe

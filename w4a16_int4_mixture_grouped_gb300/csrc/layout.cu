@@ -1,0 +1,189 @@
+// Routing -> layout kernels (the Chord page, Figure 3): the indexed align
+// step (sorted_ids with padding sentinels), the masked row lists, the
+// contiguous m_indices, and the row gather that builds padded activations.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kAlignWarps = 16;
+
+// One CTA. Three passes over the flat routed rows f = t*top_k + j:
+//  A. per-warp histograms of experts over contiguous segments of f;
+//  B. per-expert start offsets (padded to block_m, or e*max_m when masked)
+//     plus per-(warp, expert) offsets = rows of earlier warps;
+//  C. each warp walks its segment in order, ranking equal experts within a
+//     32-row step with match.any, so rows land in ascending f per expert.
+__global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(const int32_t* __restrict__ ids, int R, int E,
+                                                                 int block_m, int max_m,
+                                                                 int32_t* __restrict__ sorted_ids,
+                                                                 int32_t* __restrict__ expert_ids,
+                                                                 int32_t* __restrict__ npp, int32_t* __restrict__ counts,
+                                                                 int32_t* __restrict__ masked_rows, int* err) {
+  extern __shared__ int smem[];
+  int* hist = smem;                     // [W][E]
+  int* cnt = hist + kAlignWarps * E;    // [E]
+  int* start = cnt + E;                 // [E + 1]
+  const bool masked = max_m > 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int seg = (R + kAlignWarps - 1) / kAlignWarps;
+  const int beg = min(R, warp * seg), end = min(R, beg + seg);
+  for (int i = beg + lane; i < end; i += 32) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
+    else set_error(err, MOE_W4A16_ERR_BAD_INDEX);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int h = hist[w * E + e];
+      hist[w * E + e] = c;
+      c += h;
+    }
+    cnt[e] = c;
+    if (counts != nullptr) counts[e] = c;
+    if (masked && c > max_m) set_error(err, MOE_W4A16_ERR_CAPACITY);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int padded = 0;
+      if (e < E) padded = masked ? max_m : ((cnt[e] + block_m - 1) / block_m) * block_m;
+      int v = padded;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+      }
+      if (e < E) start[e] = carry + v - padded;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) start[E] = carry;
+  }
+  __syncthreads();
+  for (int base = beg; base < end; base += 32) {
+    const int i = base + lane;
+    const int e = i < end ? ids[i] : -1;
+    const bool valid = e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int off = 0;
+    if (valid) off = hist[warp * E + e] + rank;
+    __syncwarp();
+    if (valid) {
+      if (lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
+      if (masked) {
+        if (off < max_m) masked_rows[start[e] + off] = i;
+      } else {
+        sorted_ids[start[e] + off] = i;
+      }
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // padding: sentinels / -1 fill and the expert of every block
+  for (int e = warp; e < E; e += kAlignWarps) {
+    const int c = masked ? min(cnt[e], max_m) : cnt[e];
+    const int s = start[e], s_end = start[e + 1];
+    for (int pos = s + c + lane; pos < s_end; pos += 32) {
+      if (masked) masked_rows[pos] = -1;
+      else sorted_ids[pos] = R;
+    }
+    if (!masked) {
+      for (int b = s / block_m + lane; b < s_end / block_m; b += 32) expert_ids[b] = e;
+    }
+  }
+  if (!masked && threadIdx.x == 0) *npp = start[E];
+}
+
+__global__ void contiguous_layout_kernel(const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ expert_ids,
+                                         const int32_t* __restrict__ npp, int R, int m_pad,
+                                         int32_t* __restrict__ m_indices, int32_t* __restrict__ row_ids) {
+  int used = *npp;
+  used = used < 0 ? 0 : (used > m_pad ? m_pad : used);
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < m_pad; p += gridDim.x * blockDim.x) {
+    int m = -1, r = -1;
+    if (p < used) {
+      const int id = sorted_ids[p];
+      if (id >= 0 && id < R) {
+        m = expert_ids[p / kContigSeg];
+        r = id;
+      }
+    }
+    m_indices[p] = m;
+    row_ids[p] = r;
+  }
+}
+
+__global__ void gather_rows_kernel(const uint4* __restrict__ src, int src_rows, int KV,
+                                   const int32_t* __restrict__ row_ids, int num_rows, int div, uint4* __restrict__ dst,
+                                   int* err) {
+  const int64_t total = static_cast<int64_t>(num_rows) * KV;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = idx / KV;
+    const int c = static_cast<int>(idx - r * KV);
+    const int id = row_ids[r];
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (id >= 0) {
+      const int s = id / div;
+      if (s < src_rows) v = src[static_cast<int64_t>(s) * KV + c];
+      else set_error(err, MOE_W4A16_ERR_BAD_INDEX);
+    }
+    dst[idx] = v;
+  }
+}
+
+cudaError_t launch_align(const int32_t* topk_ids, int R, int E, int block_m, int max_m, int32_t* sorted_ids,
+                         int32_t* expert_ids, int32_t* num_post_padded, int32_t* counts, int32_t* masked_rows,
+                         int* err, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(kAlignWarps * E + 2 * E + 1) * sizeof(int);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>((kAlignWarps * MOE_W4A16_MAX_EXPERTS + 2 * MOE_W4A16_MAX_EXPERTS + 1) * sizeof(int)));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  align_kernel<<<1, kAlignWarps * 32, smem, stream>>>(topk_ids, R, E, block_m, max_m, sorted_ids, expert_ids,
+                                                      num_post_padded, counts, masked_rows, err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_contiguous_layout(const int32_t* sorted_ids, const int32_t* expert_ids,
+                                     const int32_t* num_post_padded, int R, int m_pad, int32_t* m_indices,
+                                     int32_t* row_ids, cudaStream_t stream) {
+  const int threads = 256;
+  int blocks = (m_pad + threads - 1) / threads;
+  blocks = blocks < 1 ? 1 : (blocks > 4096 ? 4096 : blocks);
+  contiguous_layout_kernel<<<blocks, threads, 0, stream>>>(sorted_ids, expert_ids, num_post_padded, R, m_pad,
+                                                           m_indices, row_ids);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const uint16_t* src, int src_rows, int K, const int32_t* row_ids, int num_rows,
+                               int row_div, uint16_t* dst, int* err, cudaStream_t stream) {
+  const int KV = K / 8;
+  const int64_t total = static_cast<int64_t>(num_rows) * KV;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  blocks = blocks < 1 ? 1 : (blocks > 8192 ? 8192 : blocks);
+  gather_rows_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
+      reinterpret_cast<const uint4*>(src), src_rows, KV, row_ids, num_rows, row_div, reinterpret_cast<uint4*>(dst),
+      err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe
