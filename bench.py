@@ -1,0 +1,556 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A16 MoE grouped-GEMM hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one pass of the hot path over one synthetic batch. The default
+workload is the prefill MoE FFN (8192 tokens, 384 experts, top-8, hidden 7168,
+intermediate 2048, indexed layout): routing align -> gate_up GEMM with fused
+SwiGLU -> down GEMM with fused top-8 combine. Other workloads: decode_gate_up,
+decode_gate_up_masked, decode_down_combine, prefill_ffn_contiguous,
+tiny_indexed, sweep_gate_up_t{16..16384}_{uniform,zipf}.
+
+Prints one JSON line (rank 0). Timing: CUDA events on the launching stream,
+warm-up first, inputs larger than L2 (the weights streamed per step exceed
+the 129 MB L2), max over ranks. Multi-GPU runs are independent replicas.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth as S  # noqa: E402
+
+METRIC = "W4A16 MoE µs/call, TFLOP/s and weight GB/s vs GB300 roofline (decode+prefill)"
+UNIT = "us/call"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CHUNK_BYTES_PER_WEIGHT = 0.5625      # 4-bit weight + a BF16 scale per 32 weights
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+WORKLOAD_ALIASES = {
+    "prefill_ffn": ("prefill_ffn", "indexed"),
+    "prefill_ffn_contiguous": ("prefill_ffn", "contiguous"),
+    "decode_gate_up": ("decode_gate_up", "indexed"),
+    "decode_gate_up_masked": ("decode_gate_up", "masked"),
+    "decode_down_combine": ("decode_down_combine", "indexed"),
+    "tiny_indexed": ("tiny_indexed", "indexed"),
+}
+
+
+def resolve(name: str):
+    if name in WORKLOAD_ALIASES:
+        base, layout = WORKLOAD_ALIASES[name]
+        return S.get_workload(base), layout
+    return S.get_workload(name), "indexed"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm: the CUDA library
+# ---------------------------------------------------------------------------
+
+def bits_to_dev(bits: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def upload_weights(wl, which: str, mode: int, dev):
+    """Generates every expert's logical weights (synth) straight into device memory and prepares them."""
+    import w4a16_int4_mixture_grouped_gb300 as M
+    n, k = wl.gemm_shape(which)
+    qw = torch.empty((wl.num_experts, n, k // 8), dtype=torch.int32, device=dev)
+    sc = torch.empty((wl.num_experts, n, k // 32), dtype=torch.bfloat16, device=dev)
+    for e in range(wl.num_experts):
+        q, s = S.expert_weights(wl, which, e)
+        qw[e].copy_(torch.from_numpy(q))
+        sc[e].copy_(torch.from_numpy(s.view(np.int16)).view(torch.bfloat16))
+    pw = M.prepare(qw, sc, mode=mode)
+    torch.cuda.synchronize(dev)
+    del qw, sc
+    return pw
+
+
+class OurArm:
+    """Holds device inputs and runs one step of the hot path for a workload."""
+
+    def __init__(self, wl, layout: str, dev):
+        import w4a16_int4_mixture_grouped_gb300 as M
+        from w4a16_int4_mixture_grouped_gb300.pipeline import MoEFFN
+        self.M, self.wl, self.layout, self.dev = M, wl, layout, dev
+        t, e, k = wl.num_tokens, wl.num_experts, wl.top_k
+        ids, wts = S.routing(wl)
+        self.ids_np, self.wts_np = ids, wts
+        self.counts = np.bincount(ids.reshape(-1), minlength=e)
+        self.e_active = int((self.counts > 0).sum())
+        self.ids = torch.from_numpy(ids).to(dev)
+        self.wts = torch.from_numpy(wts).to(dev)
+        r = t * k
+        self.kind = wl.stage
+        if wl.stage == "ffn":
+            self.w1 = upload_weights(wl, "w1", M.MODE_GATE_UP, dev)
+            self.w2 = upload_weights(wl, "w2", M.MODE_PLAIN, dev)
+            self.a_np = S.activations(wl.seed, t, wl.hidden)
+            self.a = bits_to_dev(self.a_np, dev)
+            self.ffn = MoEFFN(self.w1, self.w2, t, k,
+                              layout=M.LAYOUT_INDEXED if layout == "indexed" else M.LAYOUT_CONTIGUOUS)
+            self.out = torch.empty((t, wl.hidden), dtype=torch.bfloat16, device=dev)
+            n1, k1 = wl.gemm_shape("w1")
+            n2, k2 = wl.gemm_shape("w2")
+            self.dominant_name = "gate_up GEMM (fused SwiGLU)"
+            self.dom_flops = 2.0 * r * k1 * n1
+            self.dom_bytes = (self.e_active * CHUNK_BYTES_PER_WEIGHT * k1 * n1 + t * k1 * 2 + r * (n1 // 2) * 2)
+            self.flops = self.dom_flops + 2.0 * r * k2 * n2
+            self.weight_bytes = self.e_active * CHUNK_BYTES_PER_WEIGHT * (k1 * n1 + k2 * n2)
+            self.bound = "tensor"
+            self.h2d = self.a_np.nbytes + ids.nbytes + wts.nbytes
+            self.d2h = t * wl.hidden * 2
+        else:
+            which = "w1" if wl.stage == "gate_up" else "w2"
+            n, kd = wl.gemm_shape(which)
+            self.n, self.kd = n, kd
+            self.w = upload_weights(wl, which, M.MODE_PLAIN, dev)
+            if wl.stage == "gate_up":
+                self.a_np = S.activations(wl.seed, t, kd)
+                self.flags = 0
+                out_rows = r
+                a_rows = t
+            else:
+                self.a_np = S.down_input(wl)
+                self.flags = M.FLAG_COMBINE | M.FLAG_A_PER_ROW
+                out_rows = t
+                a_rows = r
+            self.a = bits_to_dev(self.a_np, dev)
+            self.out = torch.empty((out_rows, n), dtype=torch.bfloat16, device=dev)
+            sched = M.plan(M.LAYOUT_INDEXED, t, k, e, n, kd)
+            self.block_m = int(sched.block_m)
+            self.kernel_family = "decode" if sched.kernel == M.KERNEL_DECODE else "prefill"
+            self.ws_small = M.workspace(t, k, n, 0, dev)
+            self.ws = M.workspace(t, k, n, self.flags, dev)
+            if layout == "masked":
+                self.max_m = wl.max_m
+                self.expected_m = max(1, int(self.counts[self.counts > 0].mean())) if self.e_active else 1
+                self.a3 = torch.empty((e, self.max_m, kd), dtype=torch.bfloat16, device=dev)
+                out_rows = e * self.max_m       # flat masked output
+                self.out = torch.empty((out_rows, n), dtype=torch.bfloat16, device=dev)
+            self.dominant_name = ("gate_up" if wl.stage == "gate_up" else "down+combine") + " GEMM"
+            self.dom_flops = 2.0 * r * kd * n
+            self.dom_bytes = (self.e_active * CHUNK_BYTES_PER_WEIGHT * kd * n + a_rows * kd * 2
+                              + out_rows * n * 2 + (r * n * 4 if self.flags & M.FLAG_COMBINE else 0))
+            self.flops = self.dom_flops
+            self.weight_bytes = self.e_active * CHUNK_BYTES_PER_WEIGHT * kd * n
+            self.bound = "hbm" if self.kernel_family == "decode" else "tensor"
+            self.h2d = self.a_np.nbytes + ids.nbytes + (wts.nbytes if self.flags else 0)
+            self.d2h = out_rows * n * 2
+        torch.cuda.synchronize(dev)
+
+    def step(self, ev=None):
+        """One pass of the hot path; ev = (start, end) events bracketing the dominant GEMM."""
+        M = self.M
+        if self.kind == "ffn":
+            return self._ffn_step(ev)
+        t, k = self.wl.num_tokens, self.wl.top_k
+        if self.layout == "masked":
+            mm, rows = M.masked_layout(self.ids, self.wl.num_experts, self.max_m, self.ws_small)
+            M.gather_rows(self.a, rows.view(-1), k, out=self.a3.view(-1, self.kd))
+            if ev:
+                ev[0].record()
+            M.masked(self.a3, mm, self.expected_m, self.w, self.ws, flags=self.flags, out=self.out)
+            if ev:
+                ev[1].record()
+            return self.out
+        s_ids, e_ids, npp, _ = M.align(self.ids, self.wl.num_experts, self.block_m, self.ws_small, with_counts=False)
+        if ev:
+            ev[0].record()
+        M.indexed(self.a, self.w, s_ids, e_ids, npp, t, k, self.block_m, self.ws, flags=self.flags,
+                  topk_weights=self.wts if self.flags else None, out=self.out)
+        if ev:
+            ev[1].record()
+        return self.out
+
+    def _ffn_step(self, ev):
+        M, f = self.M, self.ffn
+        sorted_ids, expert_ids, npp, _ = M.align(self.ids, f.e, f.block_m, f.ws_small, with_counts=False)
+        if f.layout == M.LAYOUT_INDEXED:
+            if ev:
+                ev[0].record()
+            h = M.indexed(self.a, f.w1, sorted_ids, expert_ids, npp, f.t, f.top_k, f.block_m, f.ws_small,
+                          flags=M.FLAG_SWIGLU, out=f.h)
+            if ev:
+                ev[1].record()
+            f.h = h
+            return M.indexed(h, f.w2, sorted_ids, expert_ids, npp, f.t, f.top_k, f.block_m, f.ws_down,
+                             flags=M.FLAG_COMBINE | M.FLAG_A_PER_ROW, topk_weights=self.wts, out=self.out)
+        m_idx, row_ids = M.contiguous_layout(sorted_ids, expert_ids, npp, f.r)
+        a_pad = M.gather_rows(self.a, row_ids, f.top_k)
+        if ev:
+            ev[0].record()
+        h = M.contiguous(a_pad, m_idx, f.w1, f.ws_small, flags=M.FLAG_SWIGLU)
+        if ev:
+            ev[1].record()
+        return M.contiguous(h, m_idx, f.w2, f.ws_down, flags=M.FLAG_COMBINE, row_ids=row_ids, num_tokens=f.t,
+                            top_k=f.top_k, topk_weights=self.wts, out=self.out)
+
+    def host_inputs(self):
+        a = torch.from_numpy(self.a_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        ids = torch.from_numpy(self.ids_np).pin_memory()
+        wts = torch.from_numpy(self.wts_np).pin_memory()
+        out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        return a, ids, wts, out
+
+    def e2e_step(self, host):
+        a, ids, wts, out = host
+        self.a.copy_(a, non_blocking=True)
+        self.ids.copy_(ids, non_blocking=True)
+        if self.kind == "ffn" or self.flags:
+            self.wts.copy_(wts, non_blocking=True)
+        res = self.step()
+        out.copy_(res, non_blocking=True)
+
+
+# ---------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """Times the CPU oracle on slices of the workload and scales to one call.
+
+    A slice is one routed expert with all of its rows and `channels` output
+    channels of one GEMM; a call holds E_active * N / channels slices of each
+    GEMM it runs. The combine is timed over the sampled rows and scaled by
+    tokens. Each part is scaled separately and the parts are summed.
+    """
+
+    def __init__(self, wl, channels: int = 128):
+        import oracle as O
+        self.O, self.wl, self.channels = O, wl, channels
+        ids, wts = S.routing(wl)
+        self.ids, self.wts = ids, wts
+        counts = np.bincount(ids.reshape(-1), minlength=wl.num_experts)
+        self.experts = [int(e) for e in np.argsort(-counts, kind="stable") if counts[e] > 0]
+        self.next = 0
+        self.a = S.activations(wl.seed, wl.num_tokens, wl.hidden) if wl.stage in ("gate_up", "ffn") else None
+        self.h = S.down_input(wl) if wl.stage == "down" else None
+
+    def one(self):
+        """Runs one slice of every GEMM of the workload; returns (seconds spent, estimated us per call)."""
+        O, wl, c = self.O, self.wl, self.channels
+        e = self.experts[self.next % len(self.experts)]
+        self.next += 1
+        rows = np.nonzero(self.ids.reshape(-1) == e)[0]
+        local = np.zeros_like(self.ids)              # the slice's rows all go to local expert 0
+        e_act = len(self.experts)
+        spent, us = 0.0, 0.0
+        if wl.stage in ("gate_up", "ffn"):
+            n1, _ = wl.gemm_shape("w1")
+            q, s = S.expert_weights(wl, "w1", e)
+            t0 = time.perf_counter()
+            if wl.stage == "ffn":
+                sel = np.r_[0:c // 2, n1 // 2:n1 // 2 + c // 2]
+                y = O.indexed_gemm(self.a, local, lambda _: (q[sel], s[sel]), c, rows=rows)
+                O.swiglu(y[rows])
+            else:
+                O.indexed_gemm(self.a, local, lambda _: (q[:c], s[:c]), c, rows=rows)
+            dt = time.perf_counter() - t0
+            spent += dt
+            us += dt * e_act * n1 / c * 1e6
+        if wl.stage in ("down", "ffn"):
+            n2, k2 = wl.gemm_shape("w2")
+            q, s = S.expert_weights(wl, "w2", e)
+            h = self.h if self.h is not None else np.zeros((self.ids.size, k2), dtype=np.uint16)
+            t0 = time.perf_counter()
+            O.indexed_gemm(h, local, lambda _: (q[:c], s[:c]), c, a_per_routed_row=True, rows=rows)
+            dt = time.perf_counter() - t0
+            spent += dt
+            us += dt * e_act * n2 / c * 1e6
+            tok = np.unique(rows // wl.top_k)
+            if tok.size:
+                y = np.zeros((tok.size * wl.top_k, c), dtype=np.uint16)
+                t0 = time.perf_counter()
+                O.combine(y, self.wts[tok])
+                dt = time.perf_counter() - t0
+                spent += dt
+                us += dt * (wl.num_tokens / tok.size) * (n2 / c) * 1e6
+        return spent, us
+
+    def measure(self, budget_s: float):
+        spent, us = 0.0, []
+        while spent < budget_s or not us:
+            dt, v = self.one()
+            spent += dt
+            us.append(v)
+        return float(np.mean(us)), spent, len(us)
+
+
+def sample_text(wl, channels):
+    return (f"oracle on slices of {channels} output channels of one routed expert (all of its rows) per GEMM, "
+            f"scaled by experts x channel slices per call")
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, wl, layout, world, rank):
+    if rank != 0:
+        return 0
+    samp = OracleSample(wl)
+    dt, _ = samp.one()
+    steps = args.steps + args.warmup
+    budget = 150.0
+    if dt * steps > budget:
+        samp.channels = max(16, int(128 * budget / (dt * steps)) // 16 * 16)
+    for _ in range(args.warmup):
+        samp.one()
+    vals, spent = [], 0.0
+    for _ in range(args.steps):
+        d, v_us = samp.one()
+        spent += d
+        vals.append(v_us)
+    v = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, layout),
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample_text(wl, samp.channels) + f"; {args.steps} timed samples, {spent:.1f} s"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(wl, layout):
+    return {"workload": wl.name, "layout": layout, "tokens": wl.num_tokens, "experts": wl.num_experts,
+            "top_k": wl.top_k, "hidden": wl.hidden, "intermediate": wl.intermediate, "stage": wl.stage,
+            "routing": wl.routing, "seed": wl.seed,
+            "l2": "inputs larger than L2: the weights streamed per step exceed the 129 MB L2"}
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="prefill_ffn")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling cases)")
+    p.add_argument("--experts", type=int, default=0, help="override the workload's expert count (profiling cases)")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    wl, layout = resolve(args.workload)
+    if args.tokens or args.experts:
+        import dataclasses
+        t = args.tokens or wl.num_tokens
+        e = args.experts or wl.num_experts
+        wl = dataclasses.replace(wl, name=f"{wl.name}_t{t}_e{e}", num_tokens=t, num_experts=e,
+                                 hot_experts=min(wl.hot_experts, e))
+    world, rank, local = dist_setup(args.gpus)
+
+    if args.impl == "reference":
+        return run_reference(args, wl, layout, world, rank)
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import w4a16_int4_mixture_grouped_gb300 as M
+    peaks, peaks_src = load_peaks()
+    arm = OurArm(wl, layout, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        arm.step()
+    torch.cuda.synchronize(dev)
+
+    # device-timed region: inputs resident in HBM
+    dom = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.2)
+    launches0 = M.launch_count()
+    t0.record(stream)
+    for i in range(args.steps):
+        arm.step(dom[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = M.launch_count() - launches0
+    clocks = sampler.stop()
+    barrier(world)
+    total_ms = t0.elapsed_time(t1)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    dom_ms = float(np.mean([a.elapsed_time(b) for a, b in dom]))
+    ms_per_step = total_ms / args.steps
+    value = total_ms * 1e3 / (args.steps * world)
+
+    # end to end through the API with host buffers (copies inside the timed region)
+    host = arm.host_inputs()
+    for _ in range(2):
+        arm.e2e_step(host)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(3, min(args.steps, 20))
+    e0.record(stream)
+    for _ in range(e_steps):
+        arm.e2e_step(host)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = e2e_ms * 1e3 / (e_steps * world)
+
+    if arm.bound == "tensor":
+        peak = peaks["bf16_tflops_sustained"]
+        achieved = arm.dom_flops / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "kernel": arm.dominant_name, "kernel_us": dom_ms * 1e3,
+                "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step)"}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = arm.dom_bytes / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": arm.dominant_name, "kernel_us": dom_ms * 1e3,
+                "peak_source": f"{peaks_src} hbm_gbs"}
+    roof["algorithmic"] = {"flops": arm.dom_flops, "bytes": arm.dom_bytes}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": config_of(wl, layout),
+        "throughput": {"tflops": arm.flops / (ms_per_step * 1e-3) / 1e12,
+                       "weight_gbs": arm.weight_bytes / (ms_per_step * 1e-3) / 1e9,
+                       "active_experts": arm.e_active},
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(arm.h2d),
+                "d2h_bytes_per_step": int(arm.d2h)},
+        "clocks": clocks,
+        "gpu_launches": int(launches),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        samp = OracleSample(wl)
+        v, spent, n = samp.measure(args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": sample_text(wl, samp.channels) + f"; {n} slices, {spent:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
