@@ -204,8 +204,9 @@ class OurArm:
             sched = M.plan(M.LAYOUT_INDEXED, t, k, e, n, kd)
             self.block_m = int(sched.block_m)
             self.kernel_family = "decode" if sched.kernel == M.KERNEL_DECODE else "prefill"
-            self.ws_small = M.workspace(t, k, n, 0, dev)
-            self.ws = M.workspace(t, k, n, self.flags, dev)
+            lay = M.LAYOUT_MASKED if layout == "masked" else M.LAYOUT_INDEXED
+            self.ws_small = M.workspace(lay, t, k, e, n, kd, self.block_m, 0, dev)
+            self.ws = M.workspace(lay, t, k, e, n, kd, self.block_m, self.flags, dev)
             if layout == "masked":
                 self.max_m = wl.max_m
                 self.expected_m = max(1, int(self.counts[self.counts > 0].mean())) if self.e_active else 1
@@ -248,27 +249,14 @@ class OurArm:
         return self.out
 
     def _ffn_step(self, ev):
-        M, f = self.M, self.ffn
-        sorted_ids, expert_ids, npp, _ = M.align(self.ids, f.e, f.block_m, f.ws_small, with_counts=False)
-        if f.layout == M.LAYOUT_INDEXED:
-            if ev:
-                ev[0].record()
-            h = M.indexed(self.a, f.w1, sorted_ids, expert_ids, npp, f.t, f.top_k, f.block_m, f.ws_small,
-                          flags=M.FLAG_SWIGLU, out=f.h)
-            if ev:
-                ev[1].record()
-            f.h = h
-            return M.indexed(h, f.w2, sorted_ids, expert_ids, npp, f.t, f.top_k, f.block_m, f.ws_down,
-                             flags=M.FLAG_COMBINE | M.FLAG_A_PER_ROW, topk_weights=self.wts, out=self.out)
-        m_idx, row_ids = M.contiguous_layout(sorted_ids, expert_ids, npp, f.r)
-        a_pad = M.gather_rows(self.a, row_ids, f.top_k)
+        f = self.ffn
+        route = f.route(self.ids)
         if ev:
             ev[0].record()
-        h = M.contiguous(a_pad, m_idx, f.w1, f.ws_small, flags=M.FLAG_SWIGLU)
+        h = f.gate_up(self.a, route)
         if ev:
             ev[1].record()
-        return M.contiguous(h, m_idx, f.w2, f.ws_down, flags=M.FLAG_COMBINE, row_ids=row_ids, num_tokens=f.t,
-                            top_k=f.top_k, topk_weights=self.wts, out=self.out)
+        return f.down(h, route, self.wts, self.out)
 
     def host_inputs(self):
         a = torch.from_numpy(self.a_np.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -445,6 +433,9 @@ def main(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layout", default="", choices=["", "indexed", "masked"],
+                   help="override the layout of a single-GEMM workload")
+    p.add_argument("--max-m", type=int, default=0, help="masked row budget per expert with --layout masked")
     p.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling cases)")
     p.add_argument("--experts", type=int, default=0, help="override the workload's expert count (profiling cases)")
     args = p.parse_args(argv)
@@ -457,6 +448,11 @@ def main(argv=None):
         e = args.experts or wl.num_experts
         wl = dataclasses.replace(wl, name=f"{wl.name}_t{t}_e{e}", num_tokens=t, num_experts=e,
                                  hot_experts=min(wl.hot_experts, e))
+    if args.layout:
+        import dataclasses
+        layout = args.layout
+        if layout == "masked" and args.max_m:
+            wl = dataclasses.replace(wl, max_m=args.max_m)
     world, rank, local = dist_setup(args.gpus)
 
     if args.impl == "reference":

@@ -85,8 +85,12 @@ enum {
                                     needs a MODE_GATE_UP weight */
   MOE_W4A16_FLAG_COMBINE = 2u,  /* out[t, :] = bf16(sum_j w[t, j] * bf16(y[t*top_k + j, :])), j ascending;
                                     needs a MODE_PLAIN weight, topk_weights and a workspace */
-  MOE_W4A16_FLAG_A_PER_ROW = 4u /* indexed only: A holds one row per routed row (row f = t*top_k + j),
+  MOE_W4A16_FLAG_A_PER_ROW = 4u, /* indexed only: A holds one row per routed row (row f = t*top_k + j),
                                     as for the down projection; default: one row per token (row f / top_k) */
+  MOE_W4A16_FLAG_A_SORTED = 8u,  /* indexed only: A holds one row per sorted_ids slot, [max_sorted, k]
+                                    (the output of a call with MOE_W4A16_FLAG_OUT_SORTED) */
+  MOE_W4A16_FLAG_OUT_SORTED = 16u /* indexed only: output row = sorted_ids slot instead of flat id,
+                                    c is [max_sorted, n] (or n/2 with SWIGLU); padding slots are not written */
 };
 
 /* GEMM kernel families (selected by moe_w4a16_plan or forced). */
@@ -230,10 +234,15 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_gather_rows(const uint16_t* src, int sr
 MOE_W4A16_API moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_experts, int n, int k, int expected_m,
                                 moe_w4a16_schedule* plan);
 
-/* Workspace bytes for a GEMM call: 256 bytes of header, plus for
- * MOE_W4A16_FLAG_COMBINE an arrival counter per (token, 256 output channels)
- * and a bf16 [num_tokens*top_k, n] staging buffer for the routed rows. */
-MOE_W4A16_API moe_w4a16_status moe_w4a16_workspace_size(int num_tokens, int top_k, int n, uint32_t flags, size_t* bytes);
+/* Workspace bytes for a GEMM call of the given layout and shape: 256 bytes of
+ * header; for an indexed call on the prefill kernel (block_m > 32) whose A is
+ * not already sorted, a bf16 [max_sorted, k] buffer into which the routed
+ * activation rows are gathered in sorted_ids order (whole rows, once) so the
+ * GEMM reads consecutive rows; for MOE_W4A16_FLAG_COMBINE an arrival counter
+ * per (token, 256 output channels, slice) and a bf16 [num_tokens*top_k, n]
+ * staging buffer for the routed rows. block_m is ignored for the grouped layouts. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_workspace_size(int layout, int num_tokens, int top_k, int num_experts, int n,
+                                                        int k, int block_m, uint32_t flags, size_t* bytes);
 
 /* Zeroes a workspace (run once after allocating it). */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_workspace_init(void* ws, size_t ws_bytes, moe_w4a16_stream_t stream);

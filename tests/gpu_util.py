@@ -63,3 +63,10 @@ def distinct_topk(rng: np.random.Generator, t: int, e: int, k: int) -> np.ndarra
 def prepare_dev(qw: np.ndarray, sc: np.ndarray, mode: int, dev):
     import w4a16_int4_mixture_grouped_gb300 as M
     return M.prepare(torch.from_numpy(qw).to(dev), bits_to_dev(sc, dev), mode=mode)
+
+
+def small_ws(dev):
+    """A zeroed header-only workspace (enough for the routing-layout calls)."""
+    import w4a16_int4_mixture_grouped_gb300 as M
+    ws = torch.zeros(M.WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
+    return ws

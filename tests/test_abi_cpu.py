@@ -73,11 +73,25 @@ def test_align_size_capacity(lib):
 
 def test_workspace_size(lib):
     out = ctypes.c_size_t(0)
-    assert lib.moe_w4a16_workspace_size(128, 8, 7168, 0, ctypes.byref(out)) == 0 and out.value == 256
-    assert lib.moe_w4a16_workspace_size(128, 8, 7168, 2, ctypes.byref(out)) == 0
+    f = lib.moe_w4a16_workspace_size
+    # masked / decode-family indexed calls: header only
+    assert f(2, 128, 8, 384, 7168, 2048, 0, 0, ctypes.byref(out)) == 0 and out.value == 256
+    assert f(0, 128, 8, 384, 7168, 2048, 32, 0, ctypes.byref(out)) == 0 and out.value == 256
+    # combine: arrival counters + routed-row staging
+    assert f(0, 128, 8, 384, 7168, 2048, 32, 2 | 4, ctypes.byref(out)) == 0
     counters = -(-(128 * 28 * 8 * 4) // 256) * 256
     y = -(-(1024 * 7168 * 2) // 256) * 256
     assert out.value == 256 + counters + y
+    # indexed on the tcgen05 family: + gathered activations [max_sorted, K]
+    cap = 8192 * 8 + 384 * 255
+    cap = -(-cap // 256) * 256
+    assert f(0, 8192, 8, 384, 4096, 7168, 256, 1, ctypes.byref(out)) == 0
+    assert out.value == 256 + cap * 7168 * 2
+    # ... unless A is already in sorted order
+    assert f(0, 8192, 8, 384, 7168, 2048, 256, 2 | 8, ctypes.byref(out)) == 0
+    counters = -(-(8192 * 28 * 8 * 4) // 256) * 256
+    assert out.value == 256 + counters + 65536 * 7168 * 2
+    assert f(5, 1, 1, 4, 256, 64, 0, 0, ctypes.byref(out)) == 1    # unknown layout
 
 
 class Desc(ctypes.Structure):
@@ -116,6 +130,9 @@ def test_gemm_host_checks_reject_before_launch(lib):
     assert _masked(lib, d, k=64) == 1                 # K differs from the prepared weight
     assert _masked(lib, d, ws_bytes=64) == 4          # workspace too small
     assert _masked(lib, d, expected_m=0) == 1         # expected_m must be positive
+    assert _masked(lib, d, flags=8) == 1              # sorted-slot flags belong to the indexed layout
+    assert _masked(lib, d, flags=4) == 1              # so does A_PER_ROW
+    assert _masked(lib, d, flags=64) == 1             # unknown flag bit
     g = _desc()
     g.group_size = 64
     assert _masked(lib, g) == 2

@@ -9,7 +9,8 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_util import bits_to_dev, dev_to_bits, distinct_topk, i32_to_dev, prepare_dev, random_acts, random_weights
+from gpu_util import (bits_to_dev, dev_to_bits, distinct_topk, i32_to_dev, prepare_dev, random_acts, random_weights,
+                      small_ws)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +56,7 @@ def test_dequant_exhaustive_table_bit_exact():
 def test_align_bit_exact(t, k, e, bm):
     rng = np.random.default_rng(t * 7 + e)
     ids = distinct_topk(rng, t, e, k) if t else np.zeros((0, k), dtype=np.int32)
-    ws = M.workspace(max(t, 1), k, 256, 0, DEV)
+    ws = small_ws(DEV)
     s_ids, e_ids, npp, counts = M.align(i32_to_dev(ids, DEV), e, bm, ws)
     ref_s, ref_e, ref_n = O.align(ids, e, bm)
     n = int(npp.item())
@@ -68,7 +69,7 @@ def test_align_bit_exact(t, k, e, bm):
 
 def test_align_one_expert_takes_everything():
     ids = np.zeros((513, 1), dtype=np.int32)
-    ws = M.workspace(513, 1, 256, 0, DEV)
+    ws = small_ws(DEV)
     s_ids, e_ids, npp, _ = M.align(i32_to_dev(ids, DEV), 4, 32, ws)
     ref_s, ref_e, ref_n = O.align(ids, 4, 32)
     assert int(npp.item()) == ref_n
@@ -79,7 +80,7 @@ def test_contiguous_and_masked_layouts_bit_exact():
     rng = np.random.default_rng(12)
     t, k, e = 200, 4, 16
     ids = distinct_topk(rng, t, e, k)
-    ws = M.workspace(t, k, 256, 0, DEV)
+    ws = small_ws(DEV)
     s_ids, e_ids, npp, _ = M.align(i32_to_dev(ids, DEV), e, 128, ws)
     m_idx, row_ids = M.contiguous_layout(s_ids, e_ids, npp, t * k)
     ref_rows, ref_m = O.contiguous_layout(ids, e)
@@ -105,7 +106,7 @@ def test_gather_rows_exact():
 
 def test_device_detects_bad_expert_ids_and_capacity():
     ids = np.array([[0, 1], [2, 99], [1, -3]], dtype=np.int32)
-    ws = M.workspace(3, 2, 256, 0, DEV)
+    ws = small_ws(DEV)
     M.align(i32_to_dev(ids, DEV), 4, 8, ws)
     assert M.get_device_error(ws) == 8        # MOE_W4A16_ERR_BAD_INDEX
     M.clear_device_error(ws)

@@ -26,7 +26,7 @@ def _indexed_run(a_bits, qw, sc, ids, block_m, mode=1, flags=0, weights=None, a_
     e = qw.shape[0]
     pw = prepare_dev(qw, sc, mode, DEV)
     f = flags | (M.FLAG_A_PER_ROW if a_per_row else 0)
-    ws = M.workspace(t, k, pw.n, f, DEV)
+    ws = M.workspace(M.LAYOUT_INDEXED, t, k, e, pw.n, pw.k, block_m, f, DEV)
     s_ids, e_ids, npp, _ = M.align(i32_to_dev(ids, DEV), e, block_m, ws)
     w_dev = torch.from_numpy(weights).to(DEV) if weights is not None else None
     out = M.indexed(bits_to_dev(a_bits, DEV), pw, s_ids, e_ids, npp, t, k, block_m, ws, flags=f, topk_weights=w_dev)
@@ -92,6 +92,34 @@ def test_indexed_down_with_combine(block_m):
     assert np.array_equal(gpu, gpu2)
 
 
+@pytest.mark.parametrize("block_m", [32, 64, 256])
+def test_indexed_sorted_slot_hand_off(block_m):
+    """gate_up with OUT_SORTED writes rows at sorted_ids slots; down with A_SORTED reads them there."""
+    rng = np.random.default_rng(200 + block_m)
+    e, t, k, hid, inter = 6, 50, 3, 256, 256
+    a = random_acts(rng, t, hid)
+    qw1, sc1 = random_weights(rng, e, 2 * inter, hid)
+    qw2, sc2 = random_weights(rng, e, hid, inter)
+    ids = distinct_topk(rng, t, e, k)
+    w = rng.uniform(0, 1, size=(t, k)).astype(np.float32)
+    ref = O.ffn(a, ids, w, lambda x: (qw1[x], sc1[x]), lambda x: (qw2[x], sc2[x]), 2 * inter, hid)
+    pw1 = prepare_dev(qw1, sc1, 2, DEV)
+    pw2 = prepare_dev(qw2, sc2, 1, DEV)
+    f1 = M.FLAG_SWIGLU | M.FLAG_OUT_SORTED
+    f2 = M.FLAG_COMBINE | M.FLAG_A_SORTED
+    ws1 = M.workspace(M.LAYOUT_INDEXED, t, k, e, pw1.n, pw1.k, block_m, f1, DEV)
+    ws2 = M.workspace(M.LAYOUT_INDEXED, t, k, e, pw2.n, pw2.k, block_m, f2, DEV)
+    s_ids, e_ids, npp, _ = M.align(i32_to_dev(ids, DEV), e, block_m, ws1)
+    h = M.indexed(bits_to_dev(a, DEV), pw1, s_ids, e_ids, npp, t, k, block_m, ws1, flags=f1)
+    n_used = int(npp.item())
+    slots = s_ids[:n_used].cpu().numpy()
+    valid = slots < t * k
+    assert_close(dev_to_bits(h)[:n_used][valid], ref["h"][slots[valid]], f"OUT_SORTED bm={block_m}")
+    out = M.indexed(h, pw2, s_ids, e_ids, npp, t, k, block_m, ws2, flags=f2, topk_weights=torch.from_numpy(w).to(DEV))
+    assert M.get_device_error(ws1) == 0 and M.get_device_error(ws2) == 0
+    assert_close(dev_to_bits(out), ref["out"], f"A_SORTED combine bm={block_m}")
+
+
 @pytest.mark.parametrize("kernel", ["decode", "prefill"])
 def test_contiguous_matches_oracle_and_ignores_poisoned_padding(kernel, monkeypatch):
     monkeypatch.setenv("MOE_W4A16_FORCE_KERNEL", kernel)
@@ -104,7 +132,7 @@ def test_contiguous_matches_oracle_and_ignores_poisoned_padding(kernel, monkeypa
     a_pad = O.gather_rows(a, row_ids, k)
     a_pad[row_ids < 0] = 0x7FC0                      # NaN in every padding row
     pw = prepare_dev(qw, sc, 1, DEV)
-    ws = M.workspace(t, k, n, 0, DEV)
+    ws = M.workspace(M.LAYOUT_CONTIGUOUS, t, k, e, n, kd, 0, 0, DEV)
     out = torch.full((a_pad.shape[0], n), 12345.0, dtype=torch.bfloat16, device=DEV)
     M.contiguous(bits_to_dev(a_pad, DEV), i32_to_dev(m_idx, DEV), pw, ws, out=out)
     assert M.get_device_error(ws) == 0
@@ -129,7 +157,7 @@ def test_masked_matches_oracle_expected_m_only_picks_launch(kernel, expected_m, 
     for ex in range(e):
         a3[ex, masked_m[ex]:] = 0x7FC0               # NaN past each count
     pw = prepare_dev(qw, sc, 1, DEV)
-    ws = M.workspace(t, k, n, 0, DEV)
+    ws = M.workspace(M.LAYOUT_MASKED, t, k, e, n, kd, 0, 0, DEV)
     out = M.masked(bits_to_dev(a3, DEV), i32_to_dev(masked_m, DEV), expected_m, pw, ws)
     assert M.get_device_error(ws) == 0
     ref, valid = O.masked_gemm(a3, masked_m, lambda x: (qw[x], sc[x]), n)
@@ -146,7 +174,7 @@ def test_masked_swiglu_and_combine(kernel, monkeypatch):
     qw, sc = random_weights(rng, e, n, kd)
     masked_m, mrows = O.masked_layout(ids, e, max_m)
     a3 = O.gather_rows(a, mrows.reshape(-1), k).reshape(e, max_m, kd)
-    ws = M.workspace(t, k, n, M.FLAG_COMBINE, DEV)
+    ws = M.workspace(M.LAYOUT_MASKED, t, k, e, n, kd, 0, M.FLAG_COMBINE, DEV)
     y = O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), n)
     # SwiGLU on a gate_up-mode weight
     pw2 = prepare_dev(qw, sc, 2, DEV)
@@ -172,7 +200,7 @@ def test_layout_equivalence_on_gpu():
     qw, sc = random_weights(rng, e, n, kd)
     y_idx = _indexed_run(a, qw, sc, ids, 32)
     pw = prepare_dev(qw, sc, 1, DEV)
-    ws = M.workspace(t, k, n, 0, DEV)
+    ws = M.workspace(M.LAYOUT_MASKED, t, k, e, n, kd, 0, 0, DEV)
     masked_m, mrows = O.masked_layout(ids, e, 32)
     a3 = O.gather_rows(a, mrows.reshape(-1), k).reshape(e, 32, kd)
     ym = dev_to_bits(M.masked(bits_to_dev(a3, DEV), i32_to_dev(masked_m, DEV), 1, pw, ws))
@@ -184,7 +212,7 @@ def test_empty_routing_is_a_no_op():
     rng = np.random.default_rng(81)
     qw, sc = random_weights(rng, 4, 256, 128)
     pw = prepare_dev(qw, sc, 1, DEV)
-    ws = M.workspace(1, 1, 256, 0, DEV)
+    ws = M.workspace(M.LAYOUT_INDEXED, 1, 1, 4, 256, 128, 32, 0, DEV)
     ids = torch.zeros((0, 2), dtype=torch.int32, device=DEV)
     s_ids, e_ids, npp, _ = M.align(ids, 4, 32, ws)
     a = torch.zeros((0, 128), dtype=torch.bfloat16, device=DEV)
@@ -200,7 +228,7 @@ def test_device_index_checks_do_not_fault():
     rng = np.random.default_rng(91)
     qw, sc = random_weights(rng, 4, 256, 128)
     pw = prepare_dev(qw, sc, 1, DEV)
-    ws = M.workspace(8, 1, 256, 0, DEV)
+    ws = M.workspace(M.LAYOUT_INDEXED, 8, 1, 4, 256, 128, 32, 0, DEV)
     a = bits_to_dev(random_acts(rng, 8, 128), DEV)
     # masked_m above the budget -> capacity error, no out-of-bounds access
     a3 = torch.zeros((4, 16, 128), dtype=torch.bfloat16, device=DEV)
@@ -223,7 +251,7 @@ def test_mode_mismatch_fails_before_launch():
     rng = np.random.default_rng(92)
     qw, sc = random_weights(rng, 2, 256, 64)
     pw = prepare_dev(qw, sc, 1, DEV)
-    ws = M.workspace(4, 1, 256, 0, DEV)
+    ws = M.workspace(M.LAYOUT_MASKED, 4, 1, 2, 256, 64, 0, 0, DEV)
     a3 = torch.zeros((2, 4, 64), dtype=torch.bfloat16, device=DEV)
     mm = torch.zeros(2, dtype=torch.int32, device=DEV)
     before = M.launch_count()

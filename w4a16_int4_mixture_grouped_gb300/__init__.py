@@ -22,7 +22,7 @@ from . import build as _build
 
 LAYOUT_INDEXED, LAYOUT_CONTIGUOUS, LAYOUT_MASKED = 0, 1, 2
 MODE_PLAIN, MODE_GATE_UP = 1, 2
-FLAG_SWIGLU, FLAG_COMBINE, FLAG_A_PER_ROW = 1, 2, 4
+FLAG_SWIGLU, FLAG_COMBINE, FLAG_A_PER_ROW, FLAG_A_SORTED, FLAG_OUT_SORTED = 1, 2, 4, 8, 16
 KERNEL_AUTO, KERNEL_DECODE, KERNEL_PREFILL = 0, 1, 2
 WS_HEADER_BYTES = 256
 
@@ -69,7 +69,7 @@ _SIGNATURES = {
     "moe_w4a16_masked_layout": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "moe_w4a16_gather_rows": (_I, [_P, _I, _I, _P, _I, _I, _P, _P, _SZ, _P]),
     "moe_w4a16_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(Schedule)]),
-    "moe_w4a16_workspace_size": (_I, [_I, _I, _I, _U32, ctypes.POINTER(_SZ)]),
+    "moe_w4a16_workspace_size": (_I, [_I, _I, _I, _I, _I, _I, _I, _U32, ctypes.POINTER(_SZ)]),
     "moe_w4a16_workspace_init": (_I, [_P, _SZ, _P]),
     "moe_w4a16_get_device_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_w4a16_clear_device_error": (_I, [_P, _P]),
@@ -219,16 +219,19 @@ def dequant_check(pw: PreparedWeight, expert: int) -> torch.Tensor:
 # workspace and errors
 # ---------------------------------------------------------------------------
 
-def workspace_size(num_tokens: int, top_k: int, n: int, flags: int = 0) -> int:
+def workspace_size(layout: int, num_tokens: int, top_k: int, num_experts: int, n: int, k: int, block_m: int = 0,
+                   flags: int = 0) -> int:
     out = _SZ(0)
-    _check(_lib.moe_w4a16_workspace_size(num_tokens, top_k, n, flags, ctypes.byref(out)), "workspace_size")
+    _check(_lib.moe_w4a16_workspace_size(layout, num_tokens, top_k, num_experts, n, k, block_m, flags,
+                                         ctypes.byref(out)), "workspace_size")
     return int(out.value)
 
 
-def workspace(num_tokens: int, top_k: int, n: int, flags: int = 0, device=None) -> torch.Tensor:
+def workspace(layout: int, num_tokens: int, top_k: int, num_experts: int, n: int, k: int, block_m: int = 0,
+              flags: int = 0, device=None) -> torch.Tensor:
     """Allocates (through torch) and zeroes a workspace for the given call shape."""
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    nbytes = workspace_size(num_tokens, top_k, n, flags)
+    nbytes = workspace_size(layout, num_tokens, top_k, num_experts, n, k, block_m, flags)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     workspace_init(ws)
     return ws
@@ -346,7 +349,12 @@ def indexed(a: torch.Tensor, pw: PreparedWeight, sorted_ids: torch.Tensor, exper
     _need(a, "a", _BF16, dev)
     if topk_weights is not None:
         _need(topk_weights, "topk_weights", (torch.float32,), dev)
-    rows = num_tokens if flags & FLAG_COMBINE else num_tokens * top_k
+    if flags & FLAG_COMBINE:
+        rows = num_tokens
+    elif flags & FLAG_OUT_SORTED:
+        rows = sorted_ids.numel()               # one output row per sorted_ids slot
+    else:
+        rows = num_tokens * top_k
     if out is None:
         out = torch.empty((rows, _out_cols(pw, flags)), dtype=torch.bfloat16, device=dev)
     with torch.cuda.device(dev):

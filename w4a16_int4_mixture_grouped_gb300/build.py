@@ -46,8 +46,23 @@ def _deps() -> List[str]:
     return files
 
 
+def extra_flags() -> List[str]:
+    """Extra nvcc flags from MOE_W4A16_EXTRA_NVCC_FLAGS (diagnostic builds, e.g. -DMOE_W4A16_PIPE_STATS)."""
+    return os.environ.get("MOE_W4A16_EXTRA_NVCC_FLAGS", "").split()
+
+
+def _stamp() -> str:
+    return " ".join(ARCH_FLAGS + NVCC_FLAGS + extra_flags())
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB_PATH):
+        return False
+    try:
+        with open(LIB_PATH + ".flags") as fh:
+            if fh.read() != _stamp():
+                return False
+    except OSError:
         return False
     t = os.path.getmtime(LIB_PATH)
     return all(os.path.getmtime(f) <= t for f in _deps())
@@ -55,7 +70,7 @@ def up_to_date() -> bool:
 
 def _compile(nvcc: str, src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc, *ARCH_FLAGS, *NVCC_FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
+    cmd = [nvcc, *ARCH_FLAGS, *NVCC_FLAGS, *extra_flags(), "-I", INCLUDE, "-c", src, "-o", obj]
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -82,6 +97,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    with open(LIB_PATH + ".flags", "w") as fh:
+        fh.write(_stamp())
     return LIB_PATH
 
 

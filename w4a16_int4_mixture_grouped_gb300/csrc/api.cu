@@ -173,6 +173,45 @@ moe_w4a16_status moe_w4a16_align_size(int num_tokens, int top_k, int num_experts
   return MOE_W4A16_OK;
 }
 
+// Workspace of a GEMM call: [header 256 B][gathered activations][combine counters][combine staging].
+struct WsLayout {
+  size_t gather_off = 0, gather_bytes = 0;
+  size_t counters_off = 0, counters_bytes = 0;
+  size_t y_off = 0, y_bytes = 0;
+  size_t total = 0;
+};
+
+static bool gathers_activations(int layout, int block_m, uint32_t flags) {
+  return layout == MOE_W4A16_LAYOUT_INDEXED && block_m > kDecodeRows && !(flags & MOE_W4A16_FLAG_A_SORTED);
+}
+
+static moe_w4a16_status ws_layout(int layout, int num_tokens, int top_k, int num_experts, int n, int k, int block_m,
+                                  uint32_t flags, WsLayout* L) {
+  if (num_tokens < 0 || top_k < 1 || n < 1 || k < 1 || num_experts < 1 || num_experts > MOE_W4A16_MAX_EXPERTS)
+    return MOE_W4A16_ERR_INVALID_ARG;
+  if (layout < MOE_W4A16_LAYOUT_INDEXED || layout > MOE_W4A16_LAYOUT_MASKED) return MOE_W4A16_ERR_INVALID_ARG;
+  size_t off = MOE_W4A16_WS_HEADER_BYTES;
+  if (gathers_activations(layout, block_m, flags)) {
+    size_t ms, mb;
+    moe_w4a16_status st = moe_w4a16_align_size(num_tokens, top_k, num_experts, block_m, &ms, &mb);
+    if (st != MOE_W4A16_OK) return st;
+    L->gather_off = off;
+    L->gather_bytes = align_up(ms * static_cast<size_t>(k) * sizeof(uint16_t), 256);
+    off += L->gather_bytes;
+  }
+  if (flags & MOE_W4A16_FLAG_COMBINE) {
+    if (n % kGroupN) return MOE_W4A16_ERR_UNSUPPORTED;
+    L->counters_off = off;
+    L->counters_bytes = counters_bytes(num_tokens, n);
+    off += L->counters_bytes;
+    L->y_off = off;
+    L->y_bytes = align_up(static_cast<size_t>(num_tokens) * top_k * n * sizeof(uint16_t), 256);
+    off += L->y_bytes;
+  }
+  L->total = off;
+  return MOE_W4A16_OK;
+}
+
 static bool ws_ok(const void* ws, size_t ws_bytes) {
   return ws != nullptr && ws_bytes >= MOE_W4A16_WS_HEADER_BYTES && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0;
 }
@@ -292,15 +331,13 @@ moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_e
   return MOE_W4A16_OK;
 }
 
-moe_w4a16_status moe_w4a16_workspace_size(int num_tokens, int top_k, int n, uint32_t flags, size_t* bytes) {
-  if (bytes == nullptr || num_tokens < 0 || top_k < 1 || n < 1) return MOE_W4A16_ERR_INVALID_ARG;
-  size_t b = MOE_W4A16_WS_HEADER_BYTES;
-  if (flags & MOE_W4A16_FLAG_COMBINE) {
-    if (n % kGroupN) return MOE_W4A16_ERR_UNSUPPORTED;
-    b += counters_bytes(num_tokens, n);
-    b += align_up(static_cast<size_t>(num_tokens) * top_k * n * sizeof(uint16_t), 256);
-  }
-  *bytes = b;
+moe_w4a16_status moe_w4a16_workspace_size(int layout, int num_tokens, int top_k, int num_experts, int n, int k,
+                                          int block_m, uint32_t flags, size_t* bytes) {
+  if (bytes == nullptr) return MOE_W4A16_ERR_INVALID_ARG;
+  WsLayout L;
+  moe_w4a16_status st = ws_layout(layout, num_tokens, top_k, num_experts, n, k, block_m, flags, &L);
+  if (st != MOE_W4A16_OK) return st;
+  *bytes = L.total;
   return MOE_W4A16_OK;
 }
 
@@ -330,31 +367,37 @@ moe_w4a16_status moe_w4a16_clear_device_error(void* ws, moe_w4a16_stream_t strea
 // ---------------------------------------------------------------------------
 // GEMM entry points
 // ---------------------------------------------------------------------------
-static moe_w4a16_status check_gemm_common(const moe_w4a16_desc* desc, const void* prepared, const void* a, int k,
-                                          uint32_t flags, const float* topk_weights, int num_tokens, int top_k,
-                                          const void* c, const void* ws, size_t ws_bytes, bool empty = false) {
+static moe_w4a16_status check_gemm_common(int layout, int block_m, const moe_w4a16_desc* desc, const void* prepared,
+                                          const void* a, int k, uint32_t flags, const float* topk_weights,
+                                          int num_tokens, int top_k, const void* c, const void* ws, size_t ws_bytes,
+                                          WsLayout* L, bool empty = false) {
   moe_w4a16_status st = check_desc(desc, prepared);
   if (st != MOE_W4A16_OK) return st;
   if (!empty && (a == nullptr || c == nullptr)) return MOE_W4A16_ERR_INVALID_ARG;
   if (static_cast<uint32_t>(k) != desc->k) return MOE_W4A16_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(a) & 15u) || (reinterpret_cast<uintptr_t>(c) & 15u))
     return MOE_W4A16_ERR_INVALID_ARG;
-  if (flags & ~7u) return MOE_W4A16_ERR_INVALID_ARG;
+  if (flags & ~31u) return MOE_W4A16_ERR_INVALID_ARG;
+  const uint32_t indexed_only = MOE_W4A16_FLAG_A_PER_ROW | MOE_W4A16_FLAG_A_SORTED | MOE_W4A16_FLAG_OUT_SORTED;
+  if (layout != MOE_W4A16_LAYOUT_INDEXED && (flags & indexed_only)) return MOE_W4A16_ERR_INVALID_ARG;
+  if ((flags & MOE_W4A16_FLAG_A_PER_ROW) && (flags & MOE_W4A16_FLAG_A_SORTED)) return MOE_W4A16_ERR_INVALID_ARG;
+  if ((flags & MOE_W4A16_FLAG_OUT_SORTED) && (flags & MOE_W4A16_FLAG_COMBINE)) return MOE_W4A16_ERR_INVALID_ARG;
   if ((flags & MOE_W4A16_FLAG_SWIGLU) && (flags & MOE_W4A16_FLAG_COMBINE)) return MOE_W4A16_ERR_INVALID_ARG;
   if ((flags & MOE_W4A16_FLAG_SWIGLU) && desc->mode != MOE_W4A16_MODE_GATE_UP) return MOE_W4A16_ERR_MODE_MISMATCH;
   if ((flags & MOE_W4A16_FLAG_COMBINE) && desc->mode != MOE_W4A16_MODE_PLAIN) return MOE_W4A16_ERR_MODE_MISMATCH;
   if (num_tokens < 0 || top_k < 1) return MOE_W4A16_ERR_INVALID_ARG;
   if (static_cast<int64_t>(num_tokens) * top_k >= (int64_t(1) << 30)) return MOE_W4A16_ERR_UNSUPPORTED;
   if ((flags & MOE_W4A16_FLAG_COMBINE) && topk_weights == nullptr) return MOE_W4A16_ERR_INVALID_ARG;
-  size_t need = 0;
-  st = moe_w4a16_workspace_size(num_tokens, top_k, static_cast<int>(desc->n), flags, &need);
+  st = ws_layout(layout, num_tokens, top_k, static_cast<int>(desc->num_experts), static_cast<int>(desc->n), k,
+                 block_m, flags, L);
   if (st != MOE_W4A16_OK) return st;
-  if (!ws_ok(ws, ws_bytes) || ws_bytes < need) return MOE_W4A16_ERR_WORKSPACE;
+  if (!ws_ok(ws, ws_bytes) || ws_bytes < L->total) return MOE_W4A16_ERR_WORKSPACE;
   return MOE_W4A16_OK;
 }
 
 static void fill_common(GemmParams& p, const moe_w4a16_desc* desc, const void* prepared, const uint16_t* a, int k,
-                        uint32_t flags, const float* topk_weights, int num_tokens, int top_k, uint16_t* c, void* ws) {
+                        uint32_t flags, const float* topk_weights, int num_tokens, int top_k, uint16_t* c, void* ws,
+                        const WsLayout& L) {
   std::memset(&p, 0, sizeof(p));
   p.a = a;
   p.K = k;
@@ -375,9 +418,8 @@ static void fill_common(GemmParams& p, const moe_w4a16_desc* desc, const void* p
   p.c_cols = (flags & MOE_W4A16_FLAG_SWIGLU) ? p.N / 2 : p.N;
   p.err = static_cast<int*>(ws);
   if (flags & MOE_W4A16_FLAG_COMBINE) {
-    uint8_t* base = static_cast<uint8_t*>(ws) + MOE_W4A16_WS_HEADER_BYTES;
-    p.counters = reinterpret_cast<int*>(base);
-    p.y_ws = reinterpret_cast<uint16_t*>(base + counters_bytes(num_tokens, p.N));
+    p.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + L.counters_off);
+    p.y_ws = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.y_off);
   }
 }
 
@@ -401,8 +443,10 @@ moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, int k, const m
                                    const int32_t* num_post_padded, int num_tokens, int top_k, int block_m,
                                    const float* topk_weights, uint32_t flags, uint16_t* c, void* ws, size_t ws_bytes,
                                    moe_w4a16_stream_t stream) {
-  moe_w4a16_status st = check_gemm_common(desc, prepared, a, k, flags, topk_weights, num_tokens, top_k, c, ws,
-                                          ws_bytes, num_tokens == 0);
+  if (block_m < 1 || block_m > kPrefillRows) return MOE_W4A16_ERR_INVALID_ARG;
+  WsLayout L;
+  moe_w4a16_status st = check_gemm_common(MOE_W4A16_LAYOUT_INDEXED, block_m, desc, prepared, a, k, flags, topk_weights,
+                                          num_tokens, top_k, c, ws, ws_bytes, &L, num_tokens == 0);
   if (st != MOE_W4A16_OK) return st;
   if (sorted_ids == nullptr || expert_ids == nullptr || num_post_padded == nullptr) return MOE_W4A16_ERR_INVALID_ARG;
   size_t ms, mb;
@@ -410,10 +454,11 @@ moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, int k, const m
   if (st != MOE_W4A16_OK) return st;
   const int64_t r = static_cast<int64_t>(num_tokens) * top_k;
   const bool per_row = flags & MOE_W4A16_FLAG_A_PER_ROW;
-  if (a_rows != (per_row ? r : num_tokens)) return MOE_W4A16_ERR_INVALID_ARG;
+  const bool sorted_in = flags & MOE_W4A16_FLAG_A_SORTED;
+  if (a_rows != (sorted_in ? static_cast<int64_t>(ms) : (per_row ? r : num_tokens))) return MOE_W4A16_ERR_INVALID_ARG;
   if (r == 0) return MOE_W4A16_OK;
   GemmParams p;
-  fill_common(p, desc, prepared, a, k, flags, topk_weights, num_tokens, top_k, c, ws);
+  fill_common(p, desc, prepared, a, k, flags, topk_weights, num_tokens, top_k, c, ws, L);
   p.layout = MOE_W4A16_LAYOUT_INDEXED;
   p.a_rows = a_rows;
   p.sorted_ids = sorted_ids;
@@ -422,19 +467,32 @@ moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, int k, const m
   p.block_m = block_m;
   p.sorted_cap = static_cast<int64_t>(ms);
   p.a_div = per_row ? 1 : top_k;
-  p.c_rows = r;
+  p.a_sorted = sorted_in ? 1 : 0;
+  p.out_sorted = (flags & MOE_W4A16_FLAG_OUT_SORTED) ? 1 : 0;
+  p.c_rows = p.out_sorted ? static_cast<int64_t>(ms) : r;
   const int kernel = block_m <= kDecodeRows ? MOE_W4A16_KERNEL_DECODE : MOE_W4A16_KERNEL_PREFILL;
-  return run_gemm(p, kernel, num_tokens, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (gathers_activations(MOE_W4A16_LAYOUT_INDEXED, block_m, flags)) {
+    // the tcgen05 kernel reads consecutive rows: gather the routed rows once, whole, in sorted order
+    uint16_t* g = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.gather_off);
+    MOE_CUDA_TRY(launch_gather_sorted(a, a_rows, k, sorted_ids, num_post_padded, p.sorted_cap, p.R, p.a_div, g, p.err,
+                                      s));
+    p.a = g;
+    p.a_rows = p.sorted_cap;
+    p.a_div = 1;
+    p.a_sorted = 1;
+  }
+  return run_gemm(p, kernel, num_tokens, s);
 }
 
 moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad, int k, const int32_t* m_indices,
                                       const moe_w4a16_desc* desc, const void* prepared, const int32_t* row_ids,
                                       int num_tokens, int top_k, const float* topk_weights, uint32_t flags,
                                       uint16_t* c, void* ws, size_t ws_bytes, moe_w4a16_stream_t stream) {
-  moe_w4a16_status st =
-      check_gemm_common(desc, prepared, a, k, flags, topk_weights, num_tokens, top_k, c, ws, ws_bytes);
+  WsLayout L;
+  moe_w4a16_status st = check_gemm_common(MOE_W4A16_LAYOUT_CONTIGUOUS, 0, desc, prepared, a, k, flags, topk_weights,
+                                          num_tokens, top_k, c, ws, ws_bytes, &L);
   if (st != MOE_W4A16_OK) return st;
-  if (flags & MOE_W4A16_FLAG_A_PER_ROW) return MOE_W4A16_ERR_INVALID_ARG;
   if (m_indices == nullptr || m_pad < 0 || m_pad % kContigSeg != 0 || m_pad >= (1 << 30))
     return MOE_W4A16_ERR_INVALID_ARG;
   if ((flags & MOE_W4A16_FLAG_COMBINE) && row_ids == nullptr) return MOE_W4A16_ERR_INVALID_ARG;
@@ -444,7 +502,7 @@ moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad, int k, const
                       static_cast<int>(desc->n), k, 0, &pl);
   if (st != MOE_W4A16_OK) return st;
   GemmParams p;
-  fill_common(p, desc, prepared, a, k, flags, topk_weights, num_tokens, top_k, c, ws);
+  fill_common(p, desc, prepared, a, k, flags, topk_weights, num_tokens, top_k, c, ws, L);
   p.layout = MOE_W4A16_LAYOUT_CONTIGUOUS;
   p.a_rows = m_pad;
   p.m_indices = m_indices;
@@ -458,10 +516,10 @@ moe_w4a16_status moe_w4a16_masked(const uint16_t* a3, int num_experts, int max_m
                                   int expected_m, const moe_w4a16_desc* desc, const void* prepared,
                                   const int32_t* row_ids, int num_tokens, int top_k, const float* topk_weights,
                                   uint32_t flags, uint16_t* c, void* ws, size_t ws_bytes, moe_w4a16_stream_t stream) {
-  moe_w4a16_status st =
-      check_gemm_common(desc, prepared, a3, k, flags, topk_weights, num_tokens, top_k, c, ws, ws_bytes);
+  WsLayout L;
+  moe_w4a16_status st = check_gemm_common(MOE_W4A16_LAYOUT_MASKED, 0, desc, prepared, a3, k, flags, topk_weights,
+                                          num_tokens, top_k, c, ws, ws_bytes, &L);
   if (st != MOE_W4A16_OK) return st;
-  if (flags & MOE_W4A16_FLAG_A_PER_ROW) return MOE_W4A16_ERR_INVALID_ARG;
   if (masked_m == nullptr || num_experts != static_cast<int>(desc->num_experts) || max_m < 1 || expected_m < 1)
     return MOE_W4A16_ERR_INVALID_ARG;
   if (static_cast<int64_t>(num_experts) * max_m >= (int64_t(1) << 30)) return MOE_W4A16_ERR_UNSUPPORTED;
@@ -471,7 +529,7 @@ moe_w4a16_status moe_w4a16_masked(const uint16_t* a3, int num_experts, int max_m
                       expected_m, &pl);
   if (st != MOE_W4A16_OK) return st;
   GemmParams p;
-  fill_common(p, desc, prepared, a3, k, flags, topk_weights, num_tokens, top_k, c, ws);
+  fill_common(p, desc, prepared, a3, k, flags, topk_weights, num_tokens, top_k, c, ws, L);
   p.layout = MOE_W4A16_LAYOUT_MASKED;
   p.a_rows = static_cast<int64_t>(num_experts) * max_m;
   p.masked_m = masked_m;

@@ -61,12 +61,25 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // MOE_W4A16_ERR_DEVICE_TIMEOUT, raises the CTA's abort flag and returns false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// try_wait that may suspend the thread for up to `hint_ns` while the phase is incomplete.
+__device__ __forceinline__ bool mbar_test_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-      if (mbar_test(bar, parity)) return true;
+    for (int i = 0; i < 16; ++i)
+      if (mbar_test_suspend(bar, parity, 20000u)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       set_error(err, MOE_W4A16_ERR_DEVICE_TIMEOUT);
@@ -107,6 +120,30 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kWaitLimitNs) return;
   }
 }
+
+// ---------------------------------------------------------------------------
+// optional pipeline counters (diagnostic builds compiled with -DMOE_W4A16_PIPE_STATS):
+// cycles each role spends waiting or working, summed over CTAs into a device array
+// ---------------------------------------------------------------------------
+#ifdef MOE_W4A16_PIPE_STATS
+struct PipeStats {
+  unsigned long long v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  long long t = 0;
+  __device__ __forceinline__ void start() { t = clock64(); }
+  __device__ __forceinline__ void stop(int i) { v[i] += static_cast<unsigned long long>(clock64() - t); }
+  __device__ __forceinline__ void add(int i, unsigned long long x) { v[i] += x; }
+  __device__ __forceinline__ void flush(unsigned long long* dst) {
+    for (int i = 0; i < 8; ++i) atomicAdd(dst + i, v[i]);
+  }
+};
+#else
+struct PipeStats {
+  __device__ __forceinline__ void start() {}
+  __device__ __forceinline__ void stop(int) {}
+  __device__ __forceinline__ void add(int, unsigned long long) {}
+  __device__ __forceinline__ void flush(unsigned long long*) {}
+};
+#endif
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

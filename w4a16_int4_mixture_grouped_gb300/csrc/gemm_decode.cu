@@ -56,6 +56,65 @@ __device__ __forceinline__ void store_bf16(uint16_t* base, int64_t idx, float v)
   base[idx] = f32_to_bf16_rn(v);
 }
 
+// The K loop of one work unit for NT 8-row token tiles (1..4): per k-chunk
+// stage, a lane loads its four FU words of each chunk, its scales, and the
+// activation B fragments of NT tiles, releases the stage, then dequantises
+// 8 FUs and issues 8*NT MMAs. Returns false when a wait gave up.
+template <int NT>
+__device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s, int& stage, uint32_t& phase,
+                                             uint32_t wq_off, uint32_t sc_off, int lane, float (&acc)[2][4][4]) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
+  const uint32_t act_lane = 2 * kChunkBytes + (lane & 7) * kActStride + (lane >> 3) * 16;
+  for (int kc = 0; kc < p.KC; ++kc) {
+    if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) return false;
+    const uint32_t sb = s.stages + stage * kStageBytes;
+    const uint4 wq0 = lds128(sb + wq_off);
+    const uint4 wq1 = lds128(sb + kChunkBytes + wq_off);
+    const uint2 sc0 = lds64(sb + sc_off);
+    const uint2 sc1 = lds64(sb + kChunkBytes + sc_off);
+    const uint32_t w0[4] = {wq0.x, wq0.y, wq0.z, wq0.w};
+    const uint32_t w1[4] = {wq1.x, wq1.y, wq1.z, wq1.w};
+    // two halves of 32 k (= one scale group each): B fragments of the half, then its 4 FUs
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t b[NT][2][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        ldsm_x4(sb + act_lane + nt * 8 * kActStride + half * 64, b[nt][0][0], b[nt][0][1], b[nt][1][0],
+                b[nt][1][1]);
+      if (half == 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s.empty + 8 * stage);
+      }
+      uint32_t sg0, sg08, sg1, sg18;
+      scale_pairs(sc0, half, sg0, sg08);
+      scale_pairs(sc1, half, sg1, sg18);
+#pragma unroll
+      for (int kh = 0; kh < 2; ++kh) {
+        const int ks = 2 * half + kh;
+        uint32_t a0[4], a1[4];
+        dequant_fu(w0[ks], sg0, sg08, a0);
+        dequant_fu(w1[ks], sg1, sg18, a1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_16816(acc[0][nt], a0, b[nt][kh][0], b[nt][kh][1]);
+          mma_16816(acc[1][nt], a1, b[nt][kh][0], b[nt][kh][1]);
+        }
+      }
+    }
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Smem s;
@@ -148,52 +207,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
       const int ntiles = (32 - __clz(vmask) + 7) >> 3;
 
       float acc[2][4][4];
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
-
-      for (int kc = 0; kc < p.KC; ++kc) {
-        if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) goto consumer_done;
-        const uint32_t sb = s.stages + stage * kStageBytes;
-        const uint4 wq0 = lds128(sb + wq_off);
-        const uint4 wq1 = lds128(sb + kChunkBytes + wq_off);
-        const uint2 sc0 = lds64(sb + sc_off);
-        const uint2 sc1 = lds64(sb + kChunkBytes + sc_off);
-        uint32_t b[4][4][2];
-        const uint32_t act = sb + 2 * kChunkBytes + (lane & 7) * kActStride + (lane >> 3) * 16;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          if (nt < ntiles) {
-            ldsm_x4(act + nt * 8 * kActStride, b[nt][0][0], b[nt][0][1], b[nt][1][0], b[nt][1][1]);
-            ldsm_x4(act + nt * 8 * kActStride + 64, b[nt][2][0], b[nt][2][1], b[nt][3][0], b[nt][3][1]);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s.empty + 8 * stage);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        const uint32_t w0[4] = {wq0.x, wq0.y, wq0.z, wq0.w};
-        const uint32_t w1[4] = {wq1.x, wq1.y, wq1.z, wq1.w};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          uint32_t sg, sg8, a[4];
-          scale_pairs(sc0, ks >> 1, sg, sg8);
-          dequant_fu(w0[ks], sg, sg8, a);
-#pragma unroll
-          for (int nt = 0; nt < 4; ++nt)
-            if (nt < ntiles) mma_16816(acc[0][nt], a, b[nt][ks][0], b[nt][ks][1]);
-          scale_pairs(sc1, ks >> 1, sg, sg8);
-          dequant_fu(w1[ks], sg, sg8, a);
-#pragma unroll
-          for (int nt = 0; nt < 4; ++nt)
-            if (nt < ntiles) mma_16816(acc[1][nt], a, b[nt][ks][0], b[nt][ks][1]);
-        }
+      bool ok;
+      switch (ntiles) {
+        case 1: ok = consume_unit<1>(p, s, stage, phase, wq_off, sc_off, lane, acc); break;
+        case 2: ok = consume_unit<2>(p, s, stage, phase, wq_off, sc_off, lane, acc); break;
+        case 3: ok = consume_unit<3>(p, s, stage, phase, wq_off, sc_off, lane, acc); break;
+        default: ok = consume_unit<4>(p, s, stage, phase, wq_off, sc_off, lane, acc); break;
       }
+      if (!ok) goto consumer_done;
 
       // ---------------------------------------------------------- epilogue
       // acc[c][nt]: channels ch = c*128 + warp*16 + g (+8), token slots nt*8 + 2t (+1)

@@ -23,6 +23,7 @@
 // and up tiles of a unit hold matching channels in the same TMEM lane.
 // Every mbarrier wait is bounded (common.cuh); no named barrier is used after
 // the role split, so an abort can never strand a warp.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -32,11 +33,24 @@
 namespace moe {
 namespace prefill {
 
+#ifdef MOE_W4A16_PIPE_STATS
+__device__ unsigned long long g_pipe_stats[64];
+__device__ __forceinline__ unsigned long long* pipe_stats_ptr() { return g_pipe_stats; }
+#else
+__device__ __forceinline__ unsigned long long* pipe_stats_ptr() { return nullptr; }
+#endif
+
 constexpr int kThreads = 384;
 constexpr int kRows = kPrefillRows;        // 256
-constexpr int kXStages = 3;
-constexpr int kWStages = 2;
-constexpr int kPStages = 4;
+#ifndef MOE_W4A16_PREFILL_XSTAGES
+#define MOE_W4A16_PREFILL_XSTAGES 3
+#endif
+#ifndef MOE_W4A16_PREFILL_PSTAGES
+#define MOE_W4A16_PREFILL_PSTAGES 4
+#endif
+constexpr int kXStages = MOE_W4A16_PREFILL_XSTAGES;   // activation tiles (32 KB each)
+constexpr int kWStages = 2;                           // dequantised weight tiles (32 KB each)
+constexpr int kPStages = MOE_W4A16_PREFILL_PSTAGES;   // packed weight chunks (9 KB each)
 constexpr int kXBytes = kRows * 128;       // 32 KB: 256 rows x 64 k x bf16
 constexpr int kWTileBytes = kChunkN * 128; // 16 KB: 128 channels x 64 k x bf16
 constexpr int kWBytes = 2 * kWTileBytes;   // 32 KB
@@ -47,8 +61,8 @@ constexpr int kPOff = kWOff + kWStages * kWBytes;
 constexpr int kBarOff = kPOff + kPStages * kPBytes;
 constexpr int kNumBars = 2 * kPStages + 2 * kXStages + 2 * kWStages + 3;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kXRowOff = kMiscOff + 16;             // int [2][128] producer row tables
-constexpr int kPrefixOff = kXRowOff + 2 * 128 * 4;
+constexpr int kXRowOff = kMiscOff + 16;             // int [256] activation row table
+constexpr int kPrefixOff = kXRowOff + 256 * 4;
 constexpr int kTmemCols = 512;
 constexpr int kSlices = 4;                          // combine counter slices per group
 
@@ -90,6 +104,25 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// One 2-D box (64 bf16 x 16 rows, 128-byte swizzle) -> 2 KB of shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tmap, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// 4 rows of a 2-D tensor (box: 64 bf16 x 1 row, 128-byte swizzle) -> 512 B of shared memory.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tmap, int x, int y0, int y1, int y2,
+                                            int y3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+
 // K-major operand with 128-byte swizzle: rows of 128 B, 8-row atoms of 1024 B.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
@@ -106,6 +139,21 @@ __device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+#ifndef MOE_W4A16_UNIT_ORDER
+#define MOE_W4A16_UNIT_ORDER 0
+#endif
+// Work unit u -> (row block, channel group). Order 0: the groups of a block are
+// consecutive units; order 1: the blocks of a group are consecutive units.
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int nblk, int64_t u, int& blk, int& gp) {
+#if MOE_W4A16_UNIT_ORDER == 1
+  blk = static_cast<int>(u % nblk);
+  gp = static_cast<int>(u / nblk);
+#else
+  blk = static_cast<int>(u / p.NG);
+  gp = static_cast<int>(u % p.NG);
+#endif
+}
+
 // Highest valid row of a block + 1 (warp-uniform), rows scanned by a full warp.
 __device__ __forceinline__ int block_extent(const GemmParams& p, int blk, int e, int local, int rows) {
   const int lane = threadIdx.x & 31;
@@ -119,7 +167,9 @@ __device__ __forceinline__ int block_extent(const GemmParams& p, int blk, int e,
   return hi;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_tile) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -141,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
       mbar_init(p_empty + 8 * i, 8);
     }
     for (int i = 0; i < kXStages; ++i) {
-      mbar_init(x_full + 8 * i, 64);
+      mbar_init(x_full + 8 * i, 1);
       mbar_init(x_empty + 8 * i, 1);
     }
     for (int i = 0; i < kWStages; ++i) {
@@ -166,15 +216,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
                                                                         : kRows;
   const int nblk = num_row_blocks(p, rows_per_block, prefix);
   const int64_t total_units = static_cast<int64_t>(nblk) * p.NG;
+  PipeStats ps;
+  int stats_base = -1;
 
   if (warp == 0) {
     // ----------------------------------------------------- packed weights
+    stats_base = 0;
     const uint64_t pol = policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
     bool issued = false;
     for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
-      const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
+      int blk, gp;
+      unit_coords(p, nblk, u, blk, gp);
       int local;
       const int e = block_expert(p, blk, rows_per_block, prefix, local);
       if (e < 0) continue;
@@ -184,7 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
       for (int kc = 0; kc < p.KC; ++kc) {
         int ok = 1;
         if (lane == 0) {
+          ps.start();
           ok = mbar_wait(p_empty + 8 * stage, phase ^ 1u, abort_flag, p.err);
+          ps.stop(0);
           if (ok) {
             const uint32_t full = p_full + 8 * stage;
             const uint32_t dst = sbase + kPOff + stage * kPBytes;
@@ -215,10 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
     }
   } else if (warp == 1) {
     // ----------------------------------------------------- MMA issuer
+    stats_base = 8;
     int xs = 0, ws = 0;
     uint32_t xph = 0, wph = 0, aph = 0;
     for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
-      const int blk = static_cast<int>(u / p.NG);
+      int blk, gp;
+      unit_coords(p, nblk, u, blk, gp);
       int local;
       const int e = block_expert(p, blk, rows_per_block, prefix, local);
       if (e < 0) continue;
@@ -227,10 +285,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
       const int nr = (ext + 15) & ~15;
       const uint32_t idesc = idesc_bf16(128, nr);
       if (lane == 0) {
+        ps.start();
         bool ok = mbar_wait(acc_empty, aph ^ 1u, abort_flag, p.err);
+        ps.stop(0);
         tc_fence_after();
         for (int kc = 0; ok && kc < p.KC; ++kc) {
-          ok = mbar_wait(x_full + 8 * xs, xph, abort_flag, p.err) && mbar_wait(w_full + 8 * ws, wph, abort_flag, p.err);
+          ps.start();
+          ok = mbar_wait(x_full + 8 * xs, xph, abort_flag, p.err);
+          ps.stop(1);
+          ps.start();
+          ok = ok && mbar_wait(w_full + 8 * ws, wph, abort_flag, p.err);
+          ps.stop(2);
+          ps.add(3, 1);
           if (!ok) break;
           tc_fence_after();
           const uint32_t xa = sbase + kXOff + xs * kXBytes;
@@ -264,44 +330,53 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
       tc_commit(drain_bar);
       mbar_drain(drain_bar, 0);
     }
-  } else if (warp < 4) {
+  } else if (warp == 2) {
     // ----------------------------------------------------- activation rows
-    const int xw = warp - 2;                 // rows [128*xw, 128*xw + 128)
-    int* xrow = xrow_tab + xw * 128;
-    int stage = 0, prev = -1;
+    // TMA gather: one tile::gather4 copies 4 rows x 128 B into the swizzled tile;
+    // padding rows up to the 16-row MMA edge repeat row 0 (their columns are not stored).
+    stats_base = 16;
+    int* xrow = xrow_tab;
+    int stage = 0;
     uint32_t phase = 0;
+    bool issued = false;
     for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
-      const int blk = static_cast<int>(u / p.NG);
+      int blk, gp;
+      unit_coords(p, nblk, u, blk, gp);
       int local;
       const int e = block_expert(p, blk, rows_per_block, prefix, local);
       if (e < 0) continue;
       const int ext = block_extent(p, blk, e, local, rows_per_block);
       if (ext == 0) continue;
       const int nr = (ext + 15) & ~15;
+      // contiguous / masked blocks hold consecutive rows: whole 16-row boxes
+      const bool consecutive = p.layout != MOE_W4A16_LAYOUT_INDEXED || p.a_sorted;
+      const int row0 = consecutive ? block_row(p, blk, e, local, rows_per_block, 0).a_row : 0;
       __syncwarp();
-      for (int m = 0; m < 4; ++m) {
-        const int i = xw * 128 + lane + 32 * m;
-        xrow[lane + 32 * m] = (i < nr) ? block_row(p, blk, e, local, rows_per_block, i).a_row : -1;
+      if (!consecutive) {
+        for (int i = lane; i < nr; i += 32) {
+          const int ar = (i < ext) ? block_row(p, blk, e, local, rows_per_block, i).a_row : -1;
+          xrow[i] = ar < 0 ? 0 : ar;
+        }
       }
       __syncwarp();
-      const int my_rows = min(128, max(0, nr - xw * 128));
       for (int kc = 0; kc < p.KC; ++kc) {
+        ps.start();
         if (!warp_wait(x_empty + 8 * stage, phase ^ 1u, abort_flag, p.err)) goto x_done;
+        ps.stop(0);
+        const uint32_t full = x_full + 8 * stage;
+        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nr) * 128u);
+        __syncwarp();
         const uint32_t xa = sbase + kXOff + stage * kXBytes;
-        for (int idx = lane; idx < my_rows * 8; idx += 32) {
-          const int jl = idx >> 3, c = idx & 7;
-          const int j = xw * 128 + jl;
-          const int ar = xrow[jl];
-          const uint16_t* src = p.a + static_cast<int64_t>(ar < 0 ? 0 : ar) * p.K + kc * kChunkK + c * 8;
-          cp_async16(xa + j * 128 + ((c ^ (j & 7)) << 4), src, ar < 0 ? 0u : 16u);
+        if (consecutive) {
+          for (int g16 = lane; g16 < (nr >> 4); g16 += 32)
+            tma_load_2d(xa + g16 * 2048, &tmap_tile, kc * kChunkK, row0 + 16 * g16, full);
+        } else {
+          for (int g4 = lane; g4 < (nr >> 2); g4 += 32) {
+            const int* r4 = xrow + 4 * g4;
+            tma_gather4(xa + g4 * 512, &tmap_a, kc * kChunkK, r4[0], r4[1], r4[2], r4[3], full);
+          }
         }
-        cp_async_commit();
-        if (prev >= 0) {
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(x_full + 8 * prev);
-        }
-        prev = stage;
+        issued = true;
         if (++stage == kXStages) {
           stage = 0;
           phase ^= 1u;
@@ -309,11 +384,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
       }
     }
   x_done:
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (prev >= 0 && !*abort_flag) mbar_arrive(x_full + 8 * prev);
+    if (lane == 0 && *abort_flag && issued) {
+      for (int i = 0; i < kXStages; ++i) {
+        int st = stage - 1 - i;
+        uint32_t ph = phase;
+        if (st < 0) {
+          st += kXStages;
+          ph ^= 1u;
+        }
+        mbar_drain(x_full + 8 * st, ph);
+      }
+    }
+  } else if (warp == 3) {
+    // spare warp: no role
   } else {
     // ----------------------------------------------------- dequant + epilogue
+    PipeStats pst;
     const int dw = warp - 4;            // 0..7
     const int tile = dw >> 2;           // channel tile (chunk) of the unit
     const int wq = dw & 3;              // m-tiles 2wq, 2wq+1 of the tile; TMEM lane quarter
@@ -323,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
     const bool swiglu = p.flags & MOE_W4A16_FLAG_SWIGLU;
     const bool combine = p.flags & MOE_W4A16_FLAG_COMBINE;
     for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
-      const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
+      int blk, gp;
+      unit_coords(p, nblk, u, blk, gp);
       int local;
       const int e = block_expert(p, blk, rows_per_block, prefix, local);
       if (e < 0) continue;
@@ -331,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
       if (ext == 0) continue;
       const int nr = (ext + 15) & ~15;
       for (int kc = 0; kc < p.KC; ++kc) {
+        pst.start();
         if (!warp_wait(p_full + 8 * ps, pph, abort_flag, p.err)) goto d_done;
+        pst.stop(0);
         const uint32_t pa = sbase + kPOff + ps * kPBytes + tile * kChunkBytes;
         uint4 wv[2];
         uint2 sv[2];
@@ -346,7 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
           ps = 0;
           pph ^= 1u;
         }
+        pst.start();
         if (!warp_wait(w_empty + 8 * ws, wph ^ 1u, abort_flag, p.err)) goto d_done;
+        pst.stop(1);
+        pst.start();
         const uint32_t wt = sbase + kWOff + ws * kWBytes + tile * kWTileBytes;
         const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
@@ -365,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(w_full + 8 * ws);
+        pst.stop(2);
         if (++ws == kWStages) {
           ws = 0;
           wph ^= 1u;
@@ -372,7 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
       }
 
       // ------------------------------------------------- epilogue
+      pst.start();
       if (!warp_wait(acc_full, aph, abort_flag, p.err)) goto d_done;
+      pst.stop(3);
+      pst.start();
       aph ^= 1u;
       tc_fence_after();
       {
@@ -441,9 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
+      pst.stop(4);
+      pst.add(5, 1);
     }
-  d_done:;
+  d_done:
+    if (lane == 0) pst.flush(pipe_stats_ptr() + 24);
   }
+#ifdef MOE_W4A16_PIPE_STATS
+  if (lane == 0 && stats_base >= 0) ps.flush(pipe_stats_ptr() + stats_base);
+#endif
 
   tc_fence_before();
   __syncthreads();
@@ -455,8 +557,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const GemmPar
 
 }  // namespace prefill
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link needed).
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+}  // namespace
+
 cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
   using namespace prefill;
+  // activations as a 2-D tensor [a_rows, K] of bf16, read 4 rows x 128 B at a time by tile::gather4
+  EncodeTiledFn enc = encode_tiled();
+  if (enc == nullptr || p.a_rows < 1) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.a_rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkK), 1};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.a), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  // the same tensor with 16-row boxes for blocks of consecutive rows
+  CUtensorMap tmap_tile;
+  const cuuint32_t box16[2] = {static_cast<cuuint32_t>(kChunkK), 16};
+  if (enc(&tmap_tile, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.a), dims, strides, box16, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const DeviceInfo& di = device_info(device);
   const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
   const int smem = smem_bytes(prefix_entries);
@@ -475,10 +615,20 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
   int64_t grid = di.sm_count;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  prefill_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p);
+  prefill_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p, tmap, tmap_tile);
   note_launch();
   if (grid_out) *grid_out = static_cast<int>(grid);
   return cudaGetLastError();
 }
 
 }  // namespace moe
+
+#ifdef MOE_W4A16_PIPE_STATS
+// Diagnostic builds only: copies and resets the prefill kernel's pipeline counters.
+extern "C" MOE_W4A16_API int moe_w4a16_pipe_stats(unsigned long long* out, int n) {
+  if (n > 64) n = 64;
+  if (cudaMemcpyFromSymbol(out, moe::prefill::g_pipe_stats, n * sizeof(unsigned long long)) != cudaSuccess) return 7;
+  static const unsigned long long zero[64] = {0};
+  return cudaMemcpyToSymbol(moe::prefill::g_pipe_stats, zero, sizeof(zero)) == cudaSuccess ? 0 : 7;
+}
+#endif

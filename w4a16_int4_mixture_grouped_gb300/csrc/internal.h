@@ -52,6 +52,8 @@ struct GemmParams {
   int64_t sorted_cap;        // entries of sorted_ids
   int R;                     // routed rows = sentinel value
   int a_div;                 // A row = flat id / a_div
+  int a_sorted;              // A row = sorted slot (blk * block_m + i) instead of flat id / a_div
+  int out_sorted;            // output row = sorted slot instead of flat id
 
   // contiguous
   const int32_t* m_indices;
@@ -87,6 +89,10 @@ cudaError_t launch_contiguous_layout(const int32_t* sorted_ids, const int32_t* e
                                      int32_t* row_ids, cudaStream_t stream);
 cudaError_t launch_gather_rows(const uint16_t* src, int src_rows, int K, const int32_t* row_ids, int num_rows,
                                int row_div, uint16_t* dst, int* err, cudaStream_t stream);
+// dst[slot] = src[sorted_ids[slot] / row_div] for the valid slots below *num_post_padded.
+cudaError_t launch_gather_sorted(const uint16_t* src, int64_t src_rows, int K, const int32_t* sorted_ids,
+                                 const int32_t* num_post_padded, int64_t sorted_cap, int R, int row_div, uint16_t* dst,
+                                 int* err, cudaStream_t stream);
 
 // Returns the number of CTAs launched through *grid_out.
 cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out);

@@ -141,6 +141,44 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ src, int src_rows, 
   }
 }
 
+// One warp per slot: whole rows (K bf16) copied with 16-byte vectors.
+__global__ void gather_sorted_kernel(const uint4* __restrict__ src, int64_t src_rows, int KV,
+                                     const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
+                                     int64_t cap, int R, int div, uint4* __restrict__ dst, int* err) {
+  int64_t used = *npp;
+  if (used < 0 || used > cap) {
+    set_error(err, MOE_W4A16_ERR_BAD_INDEX);
+    used = used < 0 ? 0 : cap;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t slot = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); slot < used;
+       slot += warps) {
+    const int id = sorted_ids[slot];
+    if (id == R) continue;
+    if (id < 0 || id > R || id / div >= src_rows) {
+      if (lane == 0) set_error(err, MOE_W4A16_ERR_BAD_INDEX);
+      continue;
+    }
+    const uint4* s = src + static_cast<int64_t>(id / div) * KV;
+    uint4* d = dst + slot * KV;
+    for (int c = lane; c < KV; c += 32) d[c] = __ldg(s + c);
+  }
+}
+
+cudaError_t launch_gather_sorted(const uint16_t* src, int64_t src_rows, int K, const int32_t* sorted_ids,
+                                 const int32_t* num_post_padded, int64_t sorted_cap, int R, int row_div, uint16_t* dst,
+                                 int* err, cudaStream_t stream) {
+  const int threads = 256;
+  int64_t blocks = (sorted_cap + 7) / 8;
+  blocks = blocks < 1 ? 1 : (blocks > 16384 ? 16384 : blocks);
+  gather_sorted_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
+      reinterpret_cast<const uint4*>(src), src_rows, K / 8, sorted_ids, num_post_padded, sorted_cap, R, row_div,
+      reinterpret_cast<uint4*>(dst), err);
+  note_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_align(const int32_t* topk_ids, int R, int E, int block_m, int max_m, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* num_post_padded, int32_t* counts, int32_t* masked_rows,
                          int* err, cudaStream_t stream) {

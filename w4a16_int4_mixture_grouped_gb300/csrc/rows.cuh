@@ -106,13 +106,14 @@ __device__ __forceinline__ RowRef block_row(const GemmParams& p, int blk, int e,
       set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
       return r;
     }
-    const int ar = id / p.a_div;
+    const int slot = blk * p.block_m + i;
+    const int ar = p.a_sorted ? slot : id / p.a_div;
     if (ar >= p.a_rows) {
       set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
       return r;
     }
     r.a_row = ar;
-    r.out_row = id;
+    r.out_row = p.out_sorted ? slot : id;
     r.flat = id;
   } else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) {
     const int row = blk * rows + i;

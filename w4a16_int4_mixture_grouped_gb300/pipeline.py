@@ -4,6 +4,10 @@ The hot path of one MoE layer: routing layout -> gate_up GEMM with fused
 SwiGLU -> down GEMM with fused weighted top-k combine. Every step is a call
 into the CUDA library; this module only allocates buffers (through torch) and
 orders the calls on the current stream.
+
+Indexed layout: the gate_up GEMM writes SwiGLU(h) in sorted_ids slot order
+(FLAG_OUT_SORTED), so the down GEMM reads its rows consecutively
+(FLAG_A_SORTED) and combines them back per token.
 """
 
 from __future__ import annotations
@@ -12,9 +16,9 @@ from typing import Optional
 
 import torch
 
-from . import (FLAG_A_PER_ROW, FLAG_COMBINE, FLAG_SWIGLU, LAYOUT_CONTIGUOUS, LAYOUT_INDEXED, MODE_GATE_UP,
-               MODE_PLAIN, PreparedWeight, align, contiguous, contiguous_layout, gather_rows, indexed, plan,
-               workspace)
+from . import (FLAG_A_SORTED, FLAG_COMBINE, FLAG_OUT_SORTED, FLAG_SWIGLU, LAYOUT_CONTIGUOUS, LAYOUT_INDEXED,
+               MODE_GATE_UP, MODE_PLAIN, PreparedWeight, align, align_size, contiguous, contiguous_layout,
+               gather_rows, indexed, plan, workspace)
 
 CONTIGUOUS_SEGMENT = 128
 
@@ -34,32 +38,60 @@ class MoEFFN:
         self.hidden, self.inter = w1.k, w1.n // 2
         dev = w1.buffer.device
         self.device = dev
-        r = num_tokens * top_k
+        self.r = num_tokens * top_k
         if layout == LAYOUT_INDEXED:
             sched = plan(LAYOUT_INDEXED, num_tokens, top_k, self.e, w1.n, w1.k)
             self.block_m = int(block_m if block_m is not None else sched.block_m)
+            self.f1 = FLAG_SWIGLU | FLAG_OUT_SORTED
+            self.f2 = FLAG_COMBINE | FLAG_A_SORTED
+            max_sorted, _ = align_size(num_tokens, top_k, self.e, self.block_m)
+            self.h = torch.empty((max_sorted, self.inter), dtype=torch.bfloat16, device=dev)
         elif layout == LAYOUT_CONTIGUOUS:
             self.block_m = CONTIGUOUS_SEGMENT
+            self.f1, self.f2 = FLAG_SWIGLU, FLAG_COMBINE
+            self.h = None
         else:
             raise ValueError("MoEFFN runs the indexed or contiguous layout")
-        self.ws_small = workspace(num_tokens, top_k, w1.n, 0, dev)
-        self.ws_down = workspace(num_tokens, top_k, w2.n, FLAG_COMBINE, dev)
-        self.h = None
+        self.ws1 = workspace(layout, num_tokens, top_k, self.e, w1.n, w1.k, self.block_m, self.f1, dev)
+        self.ws2 = workspace(layout, num_tokens, top_k, self.e, w2.n, w2.k, self.block_m, self.f2, dev)
         self.out = torch.empty((num_tokens, self.hidden), dtype=torch.bfloat16, device=dev)
-        self.r = r
+
+    @property
+    def workspaces(self):
+        return (self.ws1, self.ws2)
+
+    def routing(self, topk_ids: torch.Tensor):
+        """The routing layout step (align) for this layer's block size."""
+        return align(topk_ids, self.e, self.block_m, self.ws1, with_counts=False)
+
+    def gate_up(self, a: torch.Tensor, route) -> torch.Tensor:
+        sorted_ids, expert_ids, npp = route[:3]
+        if self.layout == LAYOUT_INDEXED:
+            return indexed(a, self.w1, sorted_ids, expert_ids, npp, self.t, self.top_k, self.block_m, self.ws1,
+                           flags=self.f1, out=self.h)
+        m_idx, row_ids = route[3], route[4]
+        a_pad = gather_rows(a, row_ids, self.top_k)
+        return contiguous(a_pad, m_idx, self.w1, self.ws1, flags=self.f1)
+
+    def down(self, h: torch.Tensor, route, topk_weights: torch.Tensor, out: torch.Tensor) -> torch.Tensor:
+        sorted_ids, expert_ids, npp = route[:3]
+        if self.layout == LAYOUT_INDEXED:
+            return indexed(h, self.w2, sorted_ids, expert_ids, npp, self.t, self.top_k, self.block_m, self.ws2,
+                           flags=self.f2, topk_weights=topk_weights, out=out)
+        m_idx, row_ids = route[3], route[4]
+        return contiguous(h, m_idx, self.w2, self.ws2, flags=self.f2, row_ids=row_ids, num_tokens=self.t,
+                          top_k=self.top_k, topk_weights=topk_weights, out=out)
+
+    def route(self, topk_ids: torch.Tensor):
+        sorted_ids, expert_ids, npp, _ = self.routing(topk_ids)
+        if self.layout == LAYOUT_INDEXED:
+            return (sorted_ids, expert_ids, npp)
+        m_idx, row_ids = contiguous_layout(sorted_ids, expert_ids, npp, self.r)
+        return (sorted_ids, expert_ids, npp, m_idx, row_ids)
 
     def forward(self, a: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
         out = self.out if out is None else out
-        sorted_ids, expert_ids, npp, _ = align(topk_ids, self.e, self.block_m, self.ws_small, with_counts=False)
-        if self.layout == LAYOUT_INDEXED:
-            h = indexed(a, self.w1, sorted_ids, expert_ids, npp, self.t, self.top_k, self.block_m, self.ws_small,
-                        flags=FLAG_SWIGLU, out=self.h if self.h is not None and self.h.shape[0] == self.r else None)
-            self.h = h
-            return indexed(h, self.w2, sorted_ids, expert_ids, npp, self.t, self.top_k, self.block_m, self.ws_down,
-                           flags=FLAG_COMBINE | FLAG_A_PER_ROW, topk_weights=topk_weights, out=out)
-        m_idx, row_ids = contiguous_layout(sorted_ids, expert_ids, npp, self.r)
-        a_pad = gather_rows(a, row_ids, self.top_k)
-        h = contiguous(a_pad, m_idx, self.w1, self.ws_small, flags=FLAG_SWIGLU)
-        return contiguous(h, m_idx, self.w2, self.ws_down, flags=FLAG_COMBINE, row_ids=row_ids,
-                          num_tokens=self.t, top_k=self.top_k, topk_weights=topk_weights, out=out)
+        route = self.route(topk_ids)
+        h = self.gate_up(a, route)
+        return self.down(h, route, topk_weights, out)
