@@ -35,7 +35,10 @@ constexpr int kRows = kDecodeRows;                      // 32
 constexpr int kActStride = 144;                         // 128 B of k + 16 B pad (conflict-free ldmatrix)
 constexpr int kActBytes = kRows * kActStride;           // 4608
 constexpr int kStageBytes = 2 * kChunkBytes + kActBytes;  // 13824
-constexpr int kStages = 6;
+#ifndef MOE_W4A16_DECODE_STAGES
+#define MOE_W4A16_DECODE_STAGES 6
+#endif
+constexpr int kStages = MOE_W4A16_DECODE_STAGES;
 constexpr int kBarOffset = kStages * kStageBytes;
 constexpr int kMiscBytes = 256;
 constexpr int kSlices = kConsumerWarps;                 // combine counter slices per group
@@ -43,6 +46,13 @@ constexpr int kSlices = kConsumerWarps;                 // combine counter slice
 __host__ __device__ constexpr int smem_bytes(int prefix_entries) {
   return kBarOffset + kMiscBytes + prefix_entries * 4;
 }
+
+#ifdef MOE_W4A16_PIPE_STATS
+__device__ unsigned long long g_decode_stats[16];
+__device__ __forceinline__ unsigned long long* decode_stats_ptr() { return g_decode_stats; }
+#else
+__device__ __forceinline__ unsigned long long* decode_stats_ptr() { return nullptr; }
+#endif
 
 struct Smem {
   uint32_t stages;  // shared address of stage 0
@@ -62,7 +72,8 @@ __device__ __forceinline__ void store_bf16(uint16_t* base, int64_t idx, float v)
 // 8 FUs and issues 8*NT MMAs. Returns false when a wait gave up.
 template <int NT>
 __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s, int& stage, uint32_t& phase,
-                                             uint32_t wq_off, uint32_t sc_off, int lane, float (&acc)[2][4][4]) {
+                                             uint32_t wq_off, uint32_t sc_off, int lane, float (&acc)[2][4][4],
+                                             PipeStats& ps) {
 #pragma unroll
   for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -71,7 +82,10 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
       for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
   const uint32_t act_lane = 2 * kChunkBytes + (lane & 7) * kActStride + (lane >> 3) * 16;
   for (int kc = 0; kc < p.KC; ++kc) {
+    ps.start();
     if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) return false;
+    ps.stop(0);
+    ps.add(1, 1);
     const uint32_t sb = s.stages + stage * kStageBytes;
     const uint4 wq0 = lds128(sb + wq_off);
     const uint4 wq1 = lds128(sb + kChunkBytes + wq_off);
@@ -127,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(s.full + 8 * i, 1);
+      mbar_init(s.full + 8 * i, 1 + 32);  // the weight copy's expect_tx + one cp.async arrival per producer lane
       mbar_init(s.empty + 8 * i, kConsumerWarps);
     }
     *s.abort_flag = 0;
@@ -146,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
     int stage = 0;
     uint32_t phase = 0;
     bool issued_any = false;
+    PipeStats pps;
     for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
       const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
       int local;
@@ -155,20 +170,31 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
       const bool valid = rr.a_row >= 0;
       const unsigned vmask = __ballot_sync(0xffffffffu, valid);
       if (vmask == 0) continue;
-      const uint32_t tx = 2u * kChunkBytes + 128u * __popc(vmask);
-      const uint8_t* c0 = p.chunks + (static_cast<size_t>(e) * p.NB + 2 * gp) * p.KC * kChunkBytes;
-      const uint8_t* c1 = c0 + static_cast<size_t>(p.KC) * kChunkBytes;
-      const uint16_t* arow = p.a + static_cast<int64_t>(valid ? rr.a_row : 0) * p.K;
+      const uint8_t* wsrc = p.chunks + group_offset(e, gp, p.NB, p.KC);
+      // activation rows by cp.async: lane copies 16-byte piece (lane & 7) of rows (lane >> 3) + 4j
+      const uint16_t* asrc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int row = (lane >> 3) + 4 * j;
+        const int ar = __shfl_sync(0xffffffffu, rr.a_row, row);
+        asrc[j] = ar >= 0 ? p.a + static_cast<int64_t>(ar) * p.K + (lane & 7) * 8 : nullptr;
+      }
+      const uint32_t adst = 2 * kChunkBytes + (lane >> 3) * kActStride + (lane & 7) * 16;
       for (int kc = 0; kc < p.KC; ++kc) {
+        pps.start();
         if (!warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err)) goto producer_done;
+        pps.stop(0);
+        pps.add(1, 1);
         const uint32_t full = s.full + 8 * stage;
-        if (lane == 0) mbar_arrive_expect_tx(full, tx);
-        __syncwarp();
         const uint32_t sb = s.stages + stage * kStageBytes;
-        if (lane == 0) bulk_g2s_hint(sb, c0 + static_cast<size_t>(kc) * kChunkBytes, kChunkBytes, full, pol);
-        if (lane == 1)
-          bulk_g2s_hint(sb + kChunkBytes, c1 + static_cast<size_t>(kc) * kChunkBytes, kChunkBytes, full, pol);
-        if (valid) bulk_g2s(sb + 2 * kChunkBytes + lane * kActStride, arow + kc * kChunkK, 128, full);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, kPairBytes);
+          bulk_g2s_hint(sb, wsrc + static_cast<size_t>(kc) * kPairBytes, kPairBytes, full, pol);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (asrc[j] != nullptr) cp_async16(sb + adst + 4 * j * kActStride, asrc[j] + kc * kChunkK, 16);
+        cp_async_arrive_noinc(full);
         issued_any = true;
         if (++stage == kStages) {
           stage = 0;
@@ -177,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
       }
     }
   producer_done:
+    cp_async_wait<0>();
+    if (lane == 0) pps.flush(decode_stats_ptr());
     if (*s.abort_flag && issued_any) {
       // let copies already in flight land before the CTA's shared memory is released
       for (int i = 0; i < kStages; ++i) {
@@ -196,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
     uint32_t phase = 0;
     const uint32_t wq_off = (warp * 32 + lane) * 16;
     const uint32_t sc_off = kChunkWBytes + (warp * 8 + g) * 8;
+    PipeStats cps;
     for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+      cps.stop(3);   // epilogue of the previous unit (and unit bookkeeping)
       const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
       int local;
       const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
@@ -208,12 +238,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
 
       float acc[2][4][4];
       bool ok;
+      cps.start();
+      const long long t_unit = clock64();
       switch (ntiles) {
-        case 1: ok = consume_unit<1>(p, s, stage, phase, wq_off, sc_off, lane, acc); break;
-        case 2: ok = consume_unit<2>(p, s, stage, phase, wq_off, sc_off, lane, acc); break;
-        case 3: ok = consume_unit<3>(p, s, stage, phase, wq_off, sc_off, lane, acc); break;
-        default: ok = consume_unit<4>(p, s, stage, phase, wq_off, sc_off, lane, acc); break;
+        case 1: ok = consume_unit<1>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
+        case 2: ok = consume_unit<2>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
+        case 3: ok = consume_unit<3>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
+        default: ok = consume_unit<4>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
       }
+      cps.add(2, static_cast<unsigned long long>(clock64() - t_unit));
+      cps.add(4, 1);
+      cps.start();
       if (!ok) goto consumer_done;
 
       // ---------------------------------------------------------- epilogue
@@ -285,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
         }
       }
     }
-  consumer_done:;
+  consumer_done:
+    if (lane == 0) cps.flush(decode_stats_ptr() + 8);
   }
 }
 
@@ -319,3 +355,16 @@ cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t str
 }
 
 }  // namespace moe
+
+#ifdef MOE_W4A16_PIPE_STATS
+// Diagnostic builds only: copies and resets the decode kernel's pipeline counters
+// ([0] producer wait cycles, [1] stages, [8] consumer wait, [9] stages, [10] unit
+// cycles, [11] epilogue cycles, [12] units; consumer entries summed over warps).
+extern "C" MOE_W4A16_API int moe_w4a16_pipe_stats_decode(unsigned long long* out, int n) {
+  if (n > 16) n = 16;
+  if (cudaMemcpyFromSymbol(out, moe::decode::g_decode_stats, n * sizeof(unsigned long long)) != cudaSuccess)
+    return 7;
+  static const unsigned long long zero[16] = {0};
+  return cudaMemcpyToSymbol(moe::decode::g_decode_stats, zero, sizeof(zero)) == cudaSuccess ? 0 : 7;
+}
+#endif

@@ -233,8 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = block_expert(p, blk, rows_per_block, prefix, local);
       if (e < 0) continue;
       if (block_extent(p, blk, e, local, rows_per_block) == 0) continue;
-      const uint8_t* c0 = p.chunks + (static_cast<size_t>(e) * p.NB + 2 * gp) * p.KC * kChunkBytes;
-      const uint8_t* c1 = c0 + static_cast<size_t>(p.KC) * kChunkBytes;
+      const uint8_t* wsrc = p.chunks + group_offset(e, gp, p.NB, p.KC);
       for (int kc = 0; kc < p.KC; ++kc) {
         int ok = 1;
         if (lane == 0) {
@@ -245,8 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t full = p_full + 8 * stage;
             const uint32_t dst = sbase + kPOff + stage * kPBytes;
             mbar_arrive_expect_tx(full, kPBytes);
-            bulk_g2s_hint(dst, c0 + static_cast<size_t>(kc) * kChunkBytes, kChunkBytes, full, pol);
-            bulk_g2s_hint(dst + kChunkBytes, c1 + static_cast<size_t>(kc) * kChunkBytes, kChunkBytes, full, pol);
+            bulk_g2s_hint(dst, wsrc + static_cast<size_t>(kc) * kPairBytes, kPairBytes, full, pol);
             issued = true;
           }
         }

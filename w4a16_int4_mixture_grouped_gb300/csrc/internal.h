@@ -17,6 +17,17 @@ constexpr int kChunkSBytes = 512;      // 128 x 2 groups x bf16
 constexpr int kChunkBytes = kChunkWBytes + kChunkSBytes;  // 4608
 constexpr int kHeaderBytes = 256;      // prepared-buffer header
 constexpr int kGroupN = 2 * kChunkN;   // channels per GEMM work unit
+constexpr int kPairBytes = 2 * kChunkBytes;  // one k-chunk of a work unit: 9216 B
+
+// Chunk (expert e, channel block nb, k-chunk kc) of the prepared buffer, in units of
+// kChunkBytes after the header: the two blocks of a 256-channel group are adjacent.
+__host__ __device__ __forceinline__ size_t chunk_index(int e, int nb, int kc, int NB, int KC) {
+  return ((static_cast<size_t>(e) * (NB / 2) + (nb >> 1)) * KC + kc) * 2 + (nb & 1);
+}
+// First byte of the (expert, group) stream: KC consecutive 9216-byte k-chunk pairs.
+__host__ __device__ __forceinline__ size_t group_offset(int e, int gp, int NB, int KC) {
+  return chunk_index(e, 2 * gp, 0, NB, KC) * kChunkBytes;
+}
 
 
 // Counts a kernel launch (moe_w4a16_launch_count).

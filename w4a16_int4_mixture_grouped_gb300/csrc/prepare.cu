@@ -6,7 +6,9 @@
 // at model load; the forward path then reads permuted INT4 bytes and
 // MN-major scales. This layout is this library's own:
 //
-//   buffer  = 256-byte header | chunk[e][nb][kc] for e < E, nb < N/128, kc < K/64
+//   buffer  = 256-byte header | chunk[e][g][kc][h] for e < E, g < N/256, kc < K/64, h < 2
+//             (channel block nb = 2g + h: the two 128-channel blocks of a 256-channel
+//             work unit sit side by side, so one 9 KB bulk copy fetches a k-chunk)
 //   chunk   = 4096 B of nibbles | 512 B of scales            (4608 B, 16-B aligned)
 //   nibbles : uint32 word[mt][lane][ks]   (mt < 8 m-tiles of 16 channels, lane < 32,
 //             ks < 4 k-steps of 16): the FU word of common.cuh for lane (g, t) of
@@ -40,7 +42,7 @@ __global__ void __launch_bounds__(256) prepare_kernel(const int32_t* __restrict_
   const int kc = blockIdx.x, nb = blockIdx.y, e = blockIdx.z;
   const int KC = K / kChunkK, NB = N / kChunkN;
   const int KW = K / 8, KG = K / 32;
-  uint8_t* chunk = out + kHeaderBytes + ((static_cast<size_t>(e) * NB + nb) * KC + kc) * kChunkBytes;
+  uint8_t* chunk = out + kHeaderBytes + chunk_index(e, nb, kc, NB, KC) * kChunkBytes;
   const uint32_t* qe = reinterpret_cast<const uint32_t*>(qweight) + static_cast<size_t>(e) * N * KW;
   const uint16_t* se = scales + static_cast<size_t>(e) * N * KG;
 
@@ -94,8 +96,7 @@ __global__ void __launch_bounds__(256) dequant_check_kernel(const uint8_t* __res
                                                             int mode, int expert, uint16_t* __restrict__ out) {
   const int kc = blockIdx.x, nb = blockIdx.y;
   const int KC = K / kChunkK, NB = N / kChunkN;
-  const uint8_t* chunk =
-      prepared + kHeaderBytes + ((static_cast<size_t>(expert) * NB + nb) * KC + kc) * kChunkBytes;
+  const uint8_t* chunk = prepared + kHeaderBytes + chunk_index(expert, nb, kc, NB, KC) * kChunkBytes;
   const uint32_t* wq = reinterpret_cast<const uint32_t*>(chunk);
   const uint2* sc = reinterpret_cast<const uint2*>(chunk + kChunkWBytes);
   for (int widx = threadIdx.x; widx < kChunkWBytes / 4; widx += blockDim.x) {
