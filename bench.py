@@ -206,7 +206,13 @@ class OurArm:
             self.kernel_family = "decode" if sched.kernel == M.KERNEL_DECODE else "prefill"
             lay = M.LAYOUT_MASKED if layout == "masked" else M.LAYOUT_INDEXED
             self.ws_small = M.workspace(lay, t, k, e, n, kd, self.block_m, 0, dev)
-            self.ws = M.workspace(lay, t, k, e, n, kd, self.block_m, self.flags, dev)
+            gemm_flags = self.flags
+            self.a_sorted = None
+            if self.kernel_family == "prefill" and layout == "indexed":
+                gemm_flags = (self.flags & ~M.FLAG_A_PER_ROW) | M.FLAG_A_SORTED
+                max_sorted, _ = M.align_size(t, k, e, self.block_m)
+                self.a_sorted = torch.empty((max_sorted, kd), dtype=torch.bfloat16, device=dev)
+            self.ws = M.workspace(lay, t, k, e, n, kd, self.block_m, gemm_flags, dev)
             if layout == "masked":
                 self.max_m = wl.max_m
                 self.expected_m = max(1, int(self.counts[self.counts > 0].mean())) if self.e_active else 1
@@ -240,9 +246,15 @@ class OurArm:
                 ev[1].record()
             return self.out
         s_ids, e_ids, npp, _ = M.align(self.ids, self.wl.num_experts, self.block_m, self.ws_small, with_counts=False)
+        a_in, flags = self.a, self.flags
+        if self.kernel_family == "prefill":
+            # consecutive rows for the tcgen05 kernel: token rows gathered once in slot order
+            a_div = 1 if flags & M.FLAG_A_PER_ROW else k
+            a_in = M.gather_sorted(self.a, s_ids, npp, t * k, a_div, out=self.a_sorted, ws=self.ws_small)
+            flags = (flags & ~M.FLAG_A_PER_ROW) | M.FLAG_A_SORTED
         if ev:
             ev[0].record()
-        M.indexed(self.a, self.w, s_ids, e_ids, npp, t, k, self.block_m, self.ws, flags=self.flags,
+        M.indexed(a_in, self.w, s_ids, e_ids, npp, t, k, self.block_m, self.ws, flags=flags,
                   topk_weights=self.wts if self.flags else None, out=self.out)
         if ev:
             ev[1].record()
@@ -251,9 +263,10 @@ class OurArm:
     def _ffn_step(self, ev):
         f = self.ffn
         route = f.route(self.ids)
+        a_in = f.gate_up_input(self.a, route)
         if ev:
             ev[0].record()
-        h = f.gate_up(self.a, route)
+        h = f.gate_up(a_in, route)
         if ev:
             ev[1].record()
         return f.down(h, route, self.wts, self.out)

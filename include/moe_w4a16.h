@@ -219,6 +219,17 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_gather_rows(const uint16_t* src, int sr
                                        int row_div, uint16_t* dst, void* ws, size_t ws_bytes,
                                        moe_w4a16_stream_t stream);
 
+/* Activation rows in sorted_ids slot order, for MOE_W4A16_FLAG_A_SORTED calls:
+ * dst[slot, :] = src[sorted_ids[slot] / row_div, :] for every slot below
+ * *num_post_padded whose id is not the sentinel; padding slots are not written.
+ *   src bf16 [src_rows, k]; dst bf16 [max_sorted, k]; sorted_ids from moe_w4a16_align
+ *   num_rows = T*top_k (the sentinel); row_div = top_k (A per token) or 1 (A per routed row)
+ * Whole rows are copied once, so the prefill kernel then reads consecutive rows. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_gather_sorted(const uint16_t* src, int src_rows, int k,
+                                                      const int32_t* sorted_ids, const int32_t* num_post_padded,
+                                                      int max_sorted, int num_rows, int row_div, uint16_t* dst,
+                                                      void* ws, size_t ws_bytes, moe_w4a16_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Schedule and workspace (the Chord page, TL;DR: the schedule is chosen from
  * the tokens routed per expert, not the total; section "H200 prefill and TP8":

@@ -104,6 +104,24 @@ def test_gather_rows_exact():
     assert np.array_equal(dev_to_bits(out), O.gather_rows(a, row_ids, 2))
 
 
+@pytest.mark.parametrize("row_div", [1, 3])
+def test_gather_sorted_exact(row_div):
+    rng = np.random.default_rng(14)
+    t, k, e, bm, kd = 40, 3, 7, 16, 128
+    ids = distinct_topk(rng, t, e, k)
+    src = random_acts(rng, t * k if row_div == 1 else t, kd)
+    ws = small_ws(DEV)
+    s_ids, e_ids, npp, _ = M.align(i32_to_dev(ids, DEV), e, bm, ws)
+    out = torch.zeros((s_ids.numel(), kd), dtype=torch.bfloat16, device=DEV)
+    M.gather_sorted(bits_to_dev(src, DEV), s_ids, npp, t * k, row_div, out=out, ws=ws)
+    ref_s, _, n = O.align(ids, e, bm)
+    got = dev_to_bits(out)[:n]
+    valid = ref_s < t * k
+    assert np.array_equal(got[valid], src[ref_s[valid] // row_div])
+    assert np.all(got[~valid] == 0)                  # padding slots untouched
+    assert M.get_device_error(ws) == 0
+
+
 def test_device_detects_bad_expert_ids_and_capacity():
     ids = np.array([[0, 1], [2, 99], [1, -3]], dtype=np.int32)
     ws = small_ws(DEV)

@@ -68,6 +68,7 @@ _SIGNATURES = {
     "moe_w4a16_contiguous_layout": (_I, [_P, _P, _P, _I, _I, _P, _P, _P]),
     "moe_w4a16_masked_layout": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "moe_w4a16_gather_rows": (_I, [_P, _I, _I, _P, _I, _I, _P, _P, _SZ, _P]),
+    "moe_w4a16_gather_sorted": (_I, [_P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_w4a16_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(Schedule)]),
     "moe_w4a16_workspace_size": (_I, [_I, _I, _I, _I, _I, _I, _I, _U32, ctypes.POINTER(_SZ)]),
     "moe_w4a16_workspace_init": (_I, [_P, _SZ, _P]),
@@ -324,6 +325,22 @@ def gather_rows(src: torch.Tensor, row_ids: torch.Tensor, row_div: int, out: Opt
     with torch.cuda.device(dev):
         _check(_lib.moe_w4a16_gather_rows(_ptr(src), rows, k, _ptr(row_ids), n, row_div, _ptr(out), _ptr(ws),
                                           0 if ws is None else ws.numel(), _stream(dev)), "gather_rows")
+    return out
+
+
+def gather_sorted(src: torch.Tensor, sorted_ids: torch.Tensor, num_post_padded: torch.Tensor, num_rows: int,
+                  row_div: int, out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Rows of src in sorted_ids slot order: out[slot] = src[sorted_ids[slot] // row_div] (padding slots untouched)."""
+    _need(src, "src", _BF16)
+    dev = src.device
+    _need(sorted_ids, "sorted_ids", _I32, dev)
+    rows, k = src.shape
+    if out is None:
+        out = torch.empty((sorted_ids.numel(), k), dtype=src.dtype, device=dev)
+    with torch.cuda.device(dev):
+        _check(_lib.moe_w4a16_gather_sorted(_ptr(src), rows, k, _ptr(sorted_ids), _ptr(num_post_padded),
+                                            sorted_ids.numel(), num_rows, row_div, _ptr(out), _ptr(ws),
+                                            0 if ws is None else ws.numel(), _stream(dev)), "gather_sorted")
     return out
 
 

@@ -273,6 +273,21 @@ moe_w4a16_status moe_w4a16_gather_rows(const uint16_t* src, int src_rows, int k,
   return MOE_W4A16_OK;
 }
 
+moe_w4a16_status moe_w4a16_gather_sorted(const uint16_t* src, int src_rows, int k, const int32_t* sorted_ids,
+                                        const int32_t* num_post_padded, int max_sorted, int num_rows, int row_div,
+                                        uint16_t* dst, void* ws, size_t ws_bytes, moe_w4a16_stream_t stream) {
+  if (src == nullptr || sorted_ids == nullptr || num_post_padded == nullptr || dst == nullptr || src_rows < 1 ||
+      k < 8 || k % 8 != 0 || max_sorted < 0 || num_rows < 0 || row_div < 1)
+    return MOE_W4A16_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(src) & 15u) || (reinterpret_cast<uintptr_t>(dst) & 15u))
+    return MOE_W4A16_ERR_INVALID_ARG;
+  if (ws != nullptr && !ws_ok(ws, ws_bytes)) return MOE_W4A16_ERR_WORKSPACE;
+  if (max_sorted == 0) return MOE_W4A16_OK;
+  MOE_CUDA_TRY(launch_gather_sorted(src, src_rows, k, sorted_ids, num_post_padded, max_sorted, num_rows, row_div, dst,
+                                    static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_W4A16_OK;
+}
+
 moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_experts, int n, int k, int expected_m,
                                 moe_w4a16_schedule* plan) {
   if (plan == nullptr || num_tokens < 0 || top_k < 1 || num_experts < 1 || num_experts > MOE_W4A16_MAX_EXPERTS)

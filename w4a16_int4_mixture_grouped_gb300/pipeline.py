@@ -18,9 +18,10 @@ import torch
 
 from . import (FLAG_A_SORTED, FLAG_COMBINE, FLAG_OUT_SORTED, FLAG_SWIGLU, LAYOUT_CONTIGUOUS, LAYOUT_INDEXED,
                MODE_GATE_UP, MODE_PLAIN, PreparedWeight, align, align_size, contiguous, contiguous_layout,
-               gather_rows, indexed, plan, workspace)
+               gather_rows, gather_sorted, indexed, plan, workspace)
 
 CONTIGUOUS_SEGMENT = 128
+DECODE_MAX_BLOCK_M = 32    # indexed calls with block_m above this run the tcgen05 kernel
 
 
 class MoEFFN:
@@ -39,6 +40,7 @@ class MoEFFN:
         dev = w1.buffer.device
         self.device = dev
         self.r = num_tokens * top_k
+        self.a_sorted = None
         if layout == LAYOUT_INDEXED:
             sched = plan(LAYOUT_INDEXED, num_tokens, top_k, self.e, w1.n, w1.k)
             self.block_m = int(block_m if block_m is not None else sched.block_m)
@@ -46,6 +48,10 @@ class MoEFFN:
             self.f2 = FLAG_COMBINE | FLAG_A_SORTED
             max_sorted, _ = align_size(num_tokens, top_k, self.e, self.block_m)
             self.h = torch.empty((max_sorted, self.inter), dtype=torch.bfloat16, device=dev)
+            if self.block_m > DECODE_MAX_BLOCK_M:
+                # the tcgen05 family reads consecutive rows: gather the token rows once, in slot order
+                self.f1 |= FLAG_A_SORTED
+                self.a_sorted = torch.empty((max_sorted, self.hidden), dtype=torch.bfloat16, device=dev)
         elif layout == LAYOUT_CONTIGUOUS:
             self.block_m = CONTIGUOUS_SEGMENT
             self.f1, self.f2 = FLAG_SWIGLU, FLAG_COMBINE
@@ -64,14 +70,21 @@ class MoEFFN:
         """The routing layout step (align) for this layer's block size."""
         return align(topk_ids, self.e, self.block_m, self.ws1, with_counts=False)
 
-    def gate_up(self, a: torch.Tensor, route) -> torch.Tensor:
+    def gate_up_input(self, a: torch.Tensor, route) -> torch.Tensor:
+        """The gate_up GEMM's activation operand: token rows, sorted rows, or padded contiguous rows."""
         sorted_ids, expert_ids, npp = route[:3]
         if self.layout == LAYOUT_INDEXED:
-            return indexed(a, self.w1, sorted_ids, expert_ids, npp, self.t, self.top_k, self.block_m, self.ws1,
+            if self.a_sorted is None:
+                return a
+            return gather_sorted(a, sorted_ids, npp, self.r, self.top_k, out=self.a_sorted, ws=self.ws1)
+        return gather_rows(a, route[4], self.top_k)
+
+    def gate_up(self, a_in: torch.Tensor, route) -> torch.Tensor:
+        sorted_ids, expert_ids, npp = route[:3]
+        if self.layout == LAYOUT_INDEXED:
+            return indexed(a_in, self.w1, sorted_ids, expert_ids, npp, self.t, self.top_k, self.block_m, self.ws1,
                            flags=self.f1, out=self.h)
-        m_idx, row_ids = route[3], route[4]
-        a_pad = gather_rows(a, row_ids, self.top_k)
-        return contiguous(a_pad, m_idx, self.w1, self.ws1, flags=self.f1)
+        return contiguous(a_in, route[3], self.w1, self.ws1, flags=self.f1)
 
     def down(self, h: torch.Tensor, route, topk_weights: torch.Tensor, out: torch.Tensor) -> torch.Tensor:
         sorted_ids, expert_ids, npp = route[:3]
@@ -93,5 +106,5 @@ class MoEFFN:
                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
         out = self.out if out is None else out
         route = self.route(topk_ids)
-        h = self.gate_up(a, route)
+        h = self.gate_up(self.gate_up_input(a, route), route)
         return self.down(h, route, topk_weights, out)
