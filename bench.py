@@ -60,6 +60,24 @@ def resolve(name: str):
     return S.get_workload(name), "indexed"
 
 
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None when the
+    summary is missing or the kernel sources changed since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            rec = json.load(fh).get(workload_name)
+        if not rec:
+            return None
+        h = hashlib.sha256()
+        for f in rec["sources"]:
+            with open(os.path.join(ROOT, "w4a16_int4_mixture_grouped_gb300", "csrc", f), "rb") as src:
+                h.update(src.read())
+        return float(rec["dram_bytes_per_launch"]) if h.hexdigest()[:16] == rec["source_sha256"] else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -534,6 +552,9 @@ def main(argv=None):
                 "traffic": None, "kernel": arm.dominant_name, "kernel_us": dom_ms * 1e3,
                 "peak_source": f"{peaks_src} hbm_gbs"}
     roof["algorithmic"] = {"flops": arm.dom_flops, "bytes": arm.dom_bytes}
+    # DRAM bytes per launch from the committed ncu capture of this kernel and workload (null if stale or absent)
+    default_wl = args.workload if not (args.tokens or args.experts or args.layout) else None
+    roof["traffic"] = recorded_traffic(default_wl) if default_wl else None
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
