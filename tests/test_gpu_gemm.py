@@ -35,7 +35,7 @@ def _indexed_run(a_bits, qw, sc, ids, block_m, mode=1, flags=0, weights=None, a_
     return dev_to_bits(out)
 
 
-@pytest.mark.parametrize("block_m", [8, 16, 32, 48, 128, 256])
+@pytest.mark.parametrize("block_m", [8, 16, 32, 48, 128, 176, 192])
 def test_indexed_plain_matches_oracle(block_m):
     rng = np.random.default_rng(100 + block_m)
     e, t, k, kd, n = 6, 70, 3, 320, 512
@@ -47,7 +47,7 @@ def test_indexed_plain_matches_oracle(block_m):
     assert_close(gpu, ref, f"indexed bm={block_m}")
 
 
-@pytest.mark.parametrize("block_m", [32, 256])
+@pytest.mark.parametrize("block_m", [32, 192])
 @pytest.mark.parametrize("counts", [[1, 7, 8, 9, 0, 31, 32, 33], [127, 128, 129, 0, 255, 256, 257, 2], [600, 0, 0, 0]])
 def test_indexed_tile_edges(block_m, counts):
     rng = np.random.default_rng(sum(counts) + block_m)
@@ -60,7 +60,7 @@ def test_indexed_tile_edges(block_m, counts):
     assert_close(gpu, ref, f"edges bm={block_m}")
 
 
-@pytest.mark.parametrize("block_m", [32, 256])
+@pytest.mark.parametrize("block_m", [32, 192])
 def test_indexed_gate_up_mode_and_swiglu(block_m):
     rng = np.random.default_rng(7 + block_m)
     e, t, k, kd, n = 5, 90, 2, 256, 512
@@ -74,7 +74,7 @@ def test_indexed_gate_up_mode_and_swiglu(block_m):
     assert_close(h, O.swiglu(y), "fused SwiGLU")
 
 
-@pytest.mark.parametrize("block_m", [16, 32, 128, 256])
+@pytest.mark.parametrize("block_m", [16, 32, 128, 192])
 def test_indexed_down_with_combine(block_m):
     rng = np.random.default_rng(31 + block_m)
     e, t, k, kd, n = 7, 40, 4, 192, 768
@@ -92,7 +92,7 @@ def test_indexed_down_with_combine(block_m):
     assert np.array_equal(gpu, gpu2)
 
 
-@pytest.mark.parametrize("block_m", [32, 64, 256])
+@pytest.mark.parametrize("block_m", [32, 64, 192])
 def test_indexed_sorted_slot_hand_off(block_m):
     """gate_up with OUT_SORTED writes rows at sorted_ids slots; down with A_SORTED reads them there."""
     rng = np.random.default_rng(200 + block_m)

@@ -441,13 +441,20 @@ static void fill_common(GemmParams& p, const moe_w4a16_desc* desc, const void* p
 static moe_w4a16_status run_gemm(GemmParams& p, int kernel, int num_tokens, cudaStream_t stream) {
   int device = 0;
   MOE_CUDA_TRY(cudaGetDevice(&device));
-  if (p.flags & MOE_W4A16_FLAG_COMBINE) {
-    MOE_CUDA_TRY(cudaMemsetAsync(p.counters, 0, counters_bytes(num_tokens, p.N), stream));
-    p.c_rows = num_tokens;
-  }
+  const bool combine = p.flags & MOE_W4A16_FLAG_COMBINE;
+  if (combine) p.c_rows = num_tokens;
   int grid = 0;
-  if (kernel == MOE_W4A16_KERNEL_DECODE) MOE_CUDA_TRY(launch_decode_gemm(p, device, stream, &grid));
-  else MOE_CUDA_TRY(launch_prefill_gemm(p, device, stream, &grid));
+  if (kernel == MOE_W4A16_KERNEL_DECODE) {
+    // few rows: the last of a token's top_k arrivals sums its rows inside the GEMM (one launch)
+    if (combine) MOE_CUDA_TRY(cudaMemsetAsync(p.counters, 0, counters_bytes(num_tokens, p.N), stream));
+    MOE_CUDA_TRY(launch_decode_gemm(p, device, stream, &grid));
+  } else {
+    // many rows: the GEMM stages every routed row at its flat id, then one bandwidth-bound pass
+    // sums each token's top_k contiguous rows
+    MOE_CUDA_TRY(launch_prefill_gemm(p, device, stream, &grid));
+    if (combine)
+      MOE_CUDA_TRY(launch_combine_rows(p.y_ws, p.topk_weights, num_tokens, p.top_k, p.N, p.c, stream));
+  }
   return MOE_W4A16_OK;
 }
 

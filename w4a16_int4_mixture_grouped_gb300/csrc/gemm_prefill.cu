@@ -41,30 +41,34 @@ __device__ __forceinline__ unsigned long long* pipe_stats_ptr() { return nullptr
 #endif
 
 constexpr int kThreads = 384;
-constexpr int kRows = kPrefillRows;        // 256
+constexpr int kRows = kPrefillRows;        // 192: rows (MMA N) per block
 #ifndef MOE_W4A16_PREFILL_XSTAGES
-#define MOE_W4A16_PREFILL_XSTAGES 3
+#define MOE_W4A16_PREFILL_XSTAGES 5
 #endif
 #ifndef MOE_W4A16_PREFILL_PSTAGES
-#define MOE_W4A16_PREFILL_PSTAGES 4
+#define MOE_W4A16_PREFILL_PSTAGES 6
 #endif
-constexpr int kXStages = MOE_W4A16_PREFILL_XSTAGES;   // activation tiles (32 KB each)
-constexpr int kWStages = 2;                           // dequantised weight tiles (32 KB each)
+constexpr int kXStages = MOE_W4A16_PREFILL_XSTAGES;   // activation tiles (24 KB each)
+constexpr int kWStages = 2;                           // dequantised weight stages, in TMEM
 constexpr int kPStages = MOE_W4A16_PREFILL_PSTAGES;   // packed weight chunks (9 KB each)
-constexpr int kXBytes = kRows * 128;       // 32 KB: 256 rows x 64 k x bf16
-constexpr int kWTileBytes = kChunkN * 128; // 16 KB: 128 channels x 64 k x bf16
-constexpr int kWBytes = 2 * kWTileBytes;   // 32 KB
+constexpr int kXBytes = kRows * 128;       // 24 KB: 192 rows x 64 k x bf16 (multiple of 1024)
 constexpr int kPBytes = 2 * kChunkBytes;   // 9 KB
 constexpr int kXOff = 0;
-constexpr int kWOff = kXOff + kXStages * kXBytes;
-constexpr int kPOff = kWOff + kWStages * kWBytes;
+constexpr int kPOff = kXOff + kXStages * kXBytes;
 constexpr int kBarOff = kPOff + kPStages * kPBytes;
 constexpr int kNumBars = 2 * kPStages + 2 * kXStages + 2 * kWStages + 3;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kXRowOff = kMiscOff + 16;             // int [256] activation row table
-constexpr int kPrefixOff = kXRowOff + 256 * 4;
+constexpr int kXRowOff = kMiscOff + 16;             // int [kRows] activation row table
+constexpr int kPrefixOff = kXRowOff + kRows * 4;
+// TMEM (512 columns x 128 lanes x 32 bit): FP32 accumulators of the two 128-channel tiles at
+// columns [0, kRows) and [kRows, 2 kRows); dequantised BF16 weights, the MMA's A operand
+// (lane = channel, column c = k pair 2c, 2c+1), in kWStages stages of 2 tiles x 32 columns.
 constexpr int kTmemCols = 512;
-constexpr int kSlices = 4;                          // combine counter slices per group
+constexpr int kAccCols = kRows;
+constexpr int kACol0 = 2 * kAccCols;                // 384
+constexpr int kAStageCols = 2 * (kChunkK / 2);      // 64
+static_assert(kACol0 + kWStages * kAStageCols <= kTmemCols, "TMEM budget");
+static_assert(kXBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
 __host__ __device__ constexpr int smem_bytes(int prefix_entries) {
   return kPrefixOff + prefix_entries * 4 + 1024;  // + alignment slack
@@ -103,6 +107,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 16 TMEM lanes x 32 columns from the warp's MMA fragments: register pair (r[2j], r[2j+1]) lands in
+// columns 4j..4j+3, lane t/4 and t/4 + 8 (thread t) -- the A-operand fragment layout of an m16n8k16
+// MMA, so one dequantised 16x64 weight block (four k-steps) is one store.
+__device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// D += A(TMEM) * B(shared memory descriptor)
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 // One 2-D box (64 bf16 x 16 rows, 128-byte swizzle) -> 2 KB of shared memory.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tmap, int x, int y, uint32_t bar) {
@@ -298,13 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t xa = sbase + kXOff + xs * kXBytes;
-          const uint32_t wa = sbase + kWOff + ws * kWBytes;
+          const uint32_t wa = tmem + kACol0 + ws * kAStageCols;   // A operand columns of this stage
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t bdesc = sw128_desc(xa + ks * 32);
             const uint32_t acc = (kc | ks) != 0;
-            tc_mma(tmem, sw128_desc(wa + ks * 32), bdesc, idesc, acc);
-            tc_mma(tmem + 256, sw128_desc(wa + kWTileBytes + ks * 32), bdesc, idesc, acc);
+            tc_mma_ts(tmem, wa + ks * 8, bdesc, idesc, acc);
+            tc_mma_ts(tmem + kAccCols, wa + kAStageCols / 2 + ks * 8, bdesc, idesc, acc);
           }
           tc_commit(x_empty + 8 * xs);
           tc_commit(w_empty + 8 * ws);
@@ -437,22 +465,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(w_empty + 8 * ws, wph ^ 1u, abort_flag, p.err)) goto d_done;
         pst.stop(1);
         pst.start();
-        const uint32_t wt = sbase + kWOff + ws * kWBytes + tile * kWTileBytes;
-        const int mi = lane >> 3, r8 = lane & 7;
+        // A operand of this tile: TMEM lanes = channels, columns = k pairs of the 64-k chunk
+        const uint32_t at = tmem + kACol0 + ws * kAStageCols + tile * (kAStageCols / 2);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const uint32_t w4[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
-          const int n = (2 * wq + j) * 16 + (mi & 1) * 8 + r8;
+          uint32_t sg[2], sg8[2];
+          scale_pairs(sv[j], 0, sg[0], sg8[0]);
+          scale_pairs(sv[j], 1, sg[1], sg8[1]);
+          uint32_t frag[16];
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            uint32_t sg, sg8, a[4];
-            scale_pairs(sv[j], ks >> 1, sg, sg8);
-            dequant_fu(w4[ks], sg, sg8, a);
-            const int c = 2 * ks + (mi >> 1);
-            stsm_x4(wt + n * 128 + ((c ^ r8) << 4), a[0], a[1], a[2], a[3]);
+            uint32_t a[4];
+            dequant_fu(w4[ks], sg[ks >> 1], sg8[ks >> 1], a);
+            frag[4 * ks + 0] = a[0];
+            frag[4 * ks + 1] = a[1];
+            frag[4 * ks + 2] = a[2];
+            frag[4 * ks + 3] = a[3];
           }
+          // m-tile 2wq + j = TMEM lanes 32wq + 16j .. +15 (this warp's lane quarter)
+          tmem_st_16x128b_x8(at + (static_cast<uint32_t>(32 * wq + 16 * j) << 16), frag);
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(w_full + 8 * ws);
         pst.stop(2);
@@ -476,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t d0[16], d1[16];
           const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + cc * 16;
           tmem_ld16(taddr, d0);
-          tmem_ld16(taddr + 256, d1);
+          tmem_ld16(taddr + kAccCols, d1);
           tmem_wait_ld();
           RowRef rr{-1, -1, -1};
           if (lane < 16 && cc * 16 + lane < ext) rr = block_row(p, blk, e, local, rows_per_block, cc * 16 + lane);
@@ -503,33 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          if (combine) {
-            __threadfence();
-            __syncwarp();
-            int tok = -1;
-            bool last = false;
-            if (rr.a_row >= 0 && rr.flat >= 0) {
-              tok = rr.flat / p.top_k;
-              last = atomicAdd(combine_counter(p, tok, gp, q, kSlices), 1) == p.top_k - 1;
-            }
-            unsigned lm = __ballot_sync(0xffffffffu, last);
-            if (lm) __threadfence();
-            while (lm) {
-              const int src = __ffs(lm) - 1;
-              lm &= lm - 1u;
-              const int tt = __shfl_sync(0xffffffffu, tok, src);
-              float s0 = 0.f, s1 = 0.f;
-              for (int j = 0; j < p.top_k; ++j) {
-                const float w = p.topk_weights[static_cast<int64_t>(tt) * p.top_k + j];
-                const uint16_t* yr = p.y_ws + (static_cast<int64_t>(tt) * p.top_k + j) * p.N + gp * kGroupN;
-                s0 += w * bf16_to_f32(__ldcg(yr + chan));
-                s1 += w * bf16_to_f32(__ldcg(yr + kChunkN + chan));
-              }
-              uint16_t* orow_p = p.c + static_cast<int64_t>(tt) * p.N + gp * kGroupN;
-              orow_p[chan] = f32_to_bf16_rn(s0);
-              orow_p[kChunkN + chan] = f32_to_bf16_rn(s1);
-            }
-          }
+          // combine: the routed rows are staged in BF16 at their flat ids; a separate
+          // bandwidth-bound pass (combine_rows_kernel) sums each token's top_k rows
         }
       }
       tc_fence_before();

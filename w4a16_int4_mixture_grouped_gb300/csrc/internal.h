@@ -105,13 +105,17 @@ cudaError_t launch_gather_sorted(const uint16_t* src, int64_t src_rows, int K, c
                                  const int32_t* num_post_padded, int64_t sorted_cap, int R, int row_div, uint16_t* dst,
                                  int* err, cudaStream_t stream);
 
+// out[t, :] = bf16(sum_j w[t, j] * y[t*top_k + j, :]), j ascending, FP32 sums.
+cudaError_t launch_combine_rows(const uint16_t* y, const float* w, int T, int top_k, int N, uint16_t* out,
+                                cudaStream_t stream);
+
 // Returns the number of CTAs launched through *grid_out.
 cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out);
 cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out);
 
 // Rows per block the kernels use for the contiguous / masked layouts.
 constexpr int kDecodeRows = 32;
-constexpr int kPrefillRows = 256;
+constexpr int kPrefillRows = 192;   // two 128-channel accumulators of 192 columns + weight stages fill TMEM
 constexpr int kContigSeg = 128;
 
 }  // namespace moe

@@ -141,6 +141,49 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ src, int src_rows, 
   }
 }
 
+// Weighted top-k combine of staged routed rows: thread = 8 output channels of one token;
+// the top_k rows of a token are contiguous (flat ids t*top_k + j), read as 16-byte vectors.
+__global__ void combine_rows_kernel(const uint4* __restrict__ y, const float* __restrict__ w, int T, int top_k, int NV,
+                                    uint4* __restrict__ out) {
+  const int64_t total = static_cast<int64_t>(T) * NV;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = idx / NV;
+    const int c = static_cast<int>(idx - t * NV);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < top_k; ++j) {
+      const float wj = w[t * top_k + j];
+      const uint4 v = y[(t * top_k + j) * NV + c];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += wj * __uint_as_float(u[i] << 16);
+        acc[2 * i + 1] += wj * __uint_as_float(u[i] & 0xFFFF0000u);
+      }
+    }
+    uint4 r;
+    r.x = pack_bf16x2_rn(acc[0], acc[1]);
+    r.y = pack_bf16x2_rn(acc[2], acc[3]);
+    r.z = pack_bf16x2_rn(acc[4], acc[5]);
+    r.w = pack_bf16x2_rn(acc[6], acc[7]);
+    out[idx] = r;
+  }
+}
+
+cudaError_t launch_combine_rows(const uint16_t* y, const float* w, int T, int top_k, int N, uint16_t* out,
+                                cudaStream_t stream) {
+  const int NV = N / 8;
+  const int64_t total = static_cast<int64_t>(T) * NV;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  blocks = blocks > 16384 ? 16384 : blocks;
+  combine_rows_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(reinterpret_cast<const uint4*>(y), w, T,
+                                                                        top_k, NV, reinterpret_cast<uint4*>(out));
+  note_launch();
+  return cudaGetLastError();
+}
+
 // One warp per slot: whole rows (K bf16) copied with 16-byte vectors.
 __global__ void gather_sorted_kernel(const uint4* __restrict__ src, int64_t src_rows, int KV,
                                      const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
