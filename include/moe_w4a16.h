@@ -60,7 +60,8 @@ typedef enum moe_w4a16_status {
   MOE_W4A16_ERR_CAPACITY = 5,       /* device: an expert holds more rows than the masked budget */
   MOE_W4A16_ERR_DEVICE_TIMEOUT = 6, /* device: a pipeline wait gave up */
   MOE_W4A16_ERR_CUDA = 7,           /* a CUDA runtime call failed */
-  MOE_W4A16_ERR_BAD_INDEX = 8       /* device: an index array held an out-of-range value */
+  MOE_W4A16_ERR_BAD_INDEX = 8,      /* device: an index array held an out-of-range value */
+  MOE_W4A16_ERR_SCRATCH_LIMIT = 9   /* the call needs more scratch than the static array holds */
 } moe_w4a16_status;
 
 /* Activation layouts (the Chord page, section "Grouped SM90 kernels", Figure 3). */
@@ -104,6 +105,7 @@ enum {
 #define MOE_W4A16_VERSION 1u
 #define MOE_W4A16_MAX_EXPERTS 1024
 #define MOE_W4A16_WS_HEADER_BYTES 256
+#define MOE_W4A16_STATIC_SCRATCH_BYTES (16u << 20) /* scratch of moe_w4a16_indexed_noalloc */
 
 /* Host-side description of a prepared weight, filled by moe_w4a16_prepare and
  * passed by address to every GEMM call (host pointer). */
@@ -298,6 +300,36 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad
                                       const moe_w4a16_desc* desc, const void* prepared, const int32_t* row_ids,
                                       int num_tokens, int top_k, const float* topk_weights, uint32_t flags,
                                       uint16_t* c, void* ws, size_t ws_bytes, moe_w4a16_stream_t stream);
+
+/* Indexed layout on the decode kernel with NO caller workspace and NO allocation.
+ * The paper has no counterpart: this entry point exists for callers that cannot
+ * allocate device memory at call time (a custom allocator or memory pool that
+ * forbids side allocations, a runtime whose device heap is sized once at
+ * start-up, an embedding without a caching allocator to lend a workspace).
+ * It computes exactly what moe_w4a16_indexed computes for block_m 1..32, with
+ * the same arguments except the workspace, and takes its scratch (device error
+ * word, combine counters, combine staging rows) from one statically reserved
+ * device array of MOE_W4A16_STATIC_SCRATCH_BYTES (16 MiB) per device.
+ *   block_m    1..32 (decode kernel only), else INVALID_ARG
+ *   scratch    optional host pointer; receives the device address of the array,
+ *              whose first int32 is this call's device error word (read it with
+ *              moe_w4a16_get_device_error). Owned by the library: never free it.
+ * A call whose moe_w4a16_workspace_size exceeds MOE_W4A16_STATIC_SCRATCH_BYTES
+ * (with COMBINE: about 256 + 2*num_tokens*top_k*n bytes) returns
+ * MOE_W4A16_ERR_SCRATCH_LIMIT before any CUDA call. No cudaMalloc, cudaFree or
+ * allocating library routine is called.
+ * Set-up: the first call on a device, with that device current, resolves the
+ * array's address (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture.
+ * Sharing: all calls on a device share the array. Each call clears the error
+ * word and the combine counters on `stream` before its kernel; calls whose
+ * kernels overlap on the GPU race on the array (undefined results), so order
+ * them on one stream or with events. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_indexed_noalloc(const uint16_t* a, int a_rows, int k, const moe_w4a16_desc* desc,
+                                          const void* prepared, const int32_t* sorted_ids,
+                                          const int32_t* expert_ids, const int32_t* num_post_padded, int num_tokens,
+                                          int top_k, int block_m, const float* topk_weights, uint32_t flags,
+                                          uint16_t* c, void** scratch, moe_w4a16_stream_t stream);
 
 /* Masked layout (the Chord page, section "grouped operator entry points":
  * expected_m is a positive count used only to choose the launch, masked_m

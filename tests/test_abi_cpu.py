@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     lib.moe_w4a16_status_string.restype = ctypes.c_char_p
-    for s in range(9):
+    for s in range(10):
         assert lib.moe_w4a16_status_string(s)
     assert lib.moe_w4a16_status_string(99) == b"unknown status"
     lib.moe_w4a16_abi_version.restype = ctypes.c_uint32
@@ -136,6 +136,20 @@ def test_gemm_host_checks_reject_before_launch(lib):
     g = _desc()
     g.group_size = 64
     assert _masked(lib, g) == 2
+
+
+def test_noalloc_rejects_before_any_cuda_call(lib):
+    """The static-scratch entry point refuses calls whose scratch exceeds 16 MiB, and prefill block sizes."""
+    d = _desc(e=4, n=1024, k=64)
+
+    def call(t, k, block_m, flags, desc=d):
+        return lib.moe_w4a16_indexed_noalloc(FAKE, t * k, 64, ctypes.byref(desc) if desc else None, FAKE, FAKE, FAKE, FAKE, t, k, block_m, FAKE,
+                                             ctypes.c_uint32(flags), FAKE, None, None)
+
+    assert call(1100, 8, 16, 2 | 4) == 9              # 256 + counters + 1100*8*1024*2 B > 16 MiB
+    assert call(8, 8, 64, 0) == 1                     # block_m above 32 runs the prefill kernel: refused
+    assert call(8, 8, 0, 0) == 1
+    assert call(8, 8, 16, 0, desc=None) == 1
 
 
 def test_launch_counter_starts_at_zero_without_gpu(lib):

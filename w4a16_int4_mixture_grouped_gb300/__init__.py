@@ -25,10 +25,12 @@ MODE_PLAIN, MODE_GATE_UP = 1, 2
 FLAG_SWIGLU, FLAG_COMBINE, FLAG_A_PER_ROW, FLAG_A_SORTED, FLAG_OUT_SORTED = 1, 2, 4, 8, 16
 KERNEL_AUTO, KERNEL_DECODE, KERNEL_PREFILL = 0, 1, 2
 WS_HEADER_BYTES = 256
+STATIC_SCRATCH_BYTES = 16 << 20   # scratch array of indexed_noalloc, per device
 
 STATUS_NAMES = {
     0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_MODE_MISMATCH", 4: "ERR_WORKSPACE",
     5: "ERR_CAPACITY", 6: "ERR_DEVICE_TIMEOUT", 7: "ERR_CUDA", 8: "ERR_BAD_INDEX",
+    9: "ERR_SCRATCH_LIMIT",
 }
 
 
@@ -79,6 +81,8 @@ _SIGNATURES = {
     "moe_w4a16_contiguous": (_I, [_P, _I, _I, _P, ctypes.POINTER(Desc), _P, _P, _I, _I, _P, _U32, _P, _P, _SZ, _P]),
     "moe_w4a16_masked": (_I, [_P, _I, _I, _I, _P, _I, ctypes.POINTER(Desc), _P, _P, _I, _I, _P, _U32, _P, _P, _SZ,
                               _P]),
+    "moe_w4a16_indexed_noalloc": (_I, [_P, _I, _I, ctypes.POINTER(Desc), _P, _P, _P, _P, _I, _I, _I, _P, _U32, _P,
+                                       ctypes.POINTER(_P), _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -380,6 +384,25 @@ def indexed(a: torch.Tensor, pw: PreparedWeight, sorted_ids: torch.Tensor, exper
                                       block_m, _ptr(topk_weights), flags, _ptr(out), _ptr(ws), ws.numel(),
                                       _stream(dev)), "indexed")
     return out
+
+
+def indexed_noalloc(a: torch.Tensor, pw: PreparedWeight, sorted_ids: torch.Tensor, expert_ids: torch.Tensor,
+                    num_post_padded: torch.Tensor, num_tokens: int, top_k: int, block_m: int, flags: int = 0,
+                    topk_weights: Optional[torch.Tensor] = None, out: torch.Tensor = None) -> int:
+    """moe_w4a16_indexed_noalloc: the decode-kernel indexed GEMM (block_m <= 32) with the library's static
+    scratch instead of a workspace, for callers that may not allocate device memory during the call (so `out`
+    is required). Returns the device address of that scratch; its first int32 is the call's error word."""
+    dev = pw.buffer.device
+    _need(a, "a", _BF16, dev)
+    _need(out, "out", _BF16, dev)
+    scratch = ctypes.c_void_p(0)
+    with torch.cuda.device(dev):
+        _check(_lib.moe_w4a16_indexed_noalloc(_ptr(a), a.shape[0], a.shape[1], ctypes.byref(pw.desc),
+                                              _ptr(pw.buffer), _ptr(sorted_ids), _ptr(expert_ids),
+                                              _ptr(num_post_padded), num_tokens, top_k, block_m, _ptr(topk_weights),
+                                              flags, _ptr(out), ctypes.byref(scratch), _stream(dev)),
+               "indexed_noalloc")
+    return int(scratch.value or 0)
 
 
 def contiguous(a: torch.Tensor, m_indices: torch.Tensor, pw: PreparedWeight, ws: torch.Tensor, flags: int = 0,

@@ -89,6 +89,7 @@ const char* moe_w4a16_status_string(moe_w4a16_status s) {
     case MOE_W4A16_ERR_DEVICE_TIMEOUT: return "a device pipeline wait timed out";
     case MOE_W4A16_ERR_CUDA: return "CUDA runtime error";
     case MOE_W4A16_ERR_BAD_INDEX: return "index array holds an out-of-range value";
+    case MOE_W4A16_ERR_SCRATCH_LIMIT: return "call needs more scratch than the static scratch array holds";
   }
   return "unknown status";
 }
