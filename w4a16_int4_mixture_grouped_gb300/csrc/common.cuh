@@ -95,16 +95,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return mbar_wait_slow(bar, parity, abort_flag, err);
 }
 
-// Warp-uniform bounded wait: lane 0 waits and decides for the warp, so a
-// timeout never splits a warp in front of a warp-collective operation. The
-// other lanes then observe the completed phase themselves (acquire); it
-// cannot have moved on, because the next phase needs this warp's own release.
+static __device__ __noinline__ bool warp_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                   int* err) {
+  const bool leader = (threadIdx.x & 31) == 0;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (__all_sync(0xffffffffu, mbar_test_suspend(bar, parity, 20000u))) return true;
+    int stop = 0;
+    if (leader) {
+      if (abort_flag != nullptr && *abort_flag) {
+        stop = 1;
+      } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+        set_error(err, MOE_W4A16_ERR_DEVICE_TIMEOUT);
+        if (abort_flag != nullptr) *abort_flag = 1;
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+  }
+}
+
+// Warp-uniform bounded wait: every lane tests the phase itself (so every lane
+// acquires), and the warp proceeds only when all lanes saw it complete; the
+// give-up decision is lane 0's, broadcast, so a timeout never splits a warp in
+// front of a warp-collective operation. A completed phase cannot move on
+// under a lane, because the next phase needs this warp's own release.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, err);
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok && (threadIdx.x & 31) != 0) ok = mbar_wait(bar, parity, nullptr, err);
-  return __all_sync(0xffffffffu, ok) != 0;
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  return warp_wait_slow(bar, parity, abort_flag, err);
 }
 
 // Warp-uniform read of the CTA's abort flag.
