@@ -243,7 +243,9 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_gather_sorted(const uint16_t* src, int 
  * tok_e = T*top_k/E (indexed), m_pad/E (contiguous) or expected_m (masked,
  * a positive count used only to choose the launch; results never depend on
  * it). The environment variable MOE_W4A16_FORCE_KERNEL=decode|prefill
- * overrides the family (read on every call, part of the memo key). `plan` is host. */
+ * overrides the family (read on every call, part of the memo key). Indexed
+ * block_m: 16 for the decode family at tok_e <= 4, 32 for the rest of the
+ * decode family, 192 for the prefill family. `plan` is host. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_experts, int n, int k, int expected_m,
                                 moe_w4a16_schedule* plan);
 
@@ -280,7 +282,7 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_clear_device_error(void* ws, moe_w4a16_
  * the routing index; section "Indexed kernels").
  *   a          bf16 [a_rows, k]: a_rows = T, or T*top_k with MOE_W4A16_FLAG_A_PER_ROW
  *   sorted_ids, expert_ids, num_post_padded: from moe_w4a16_align with this block_m
- *   block_m    1..32 runs the decode kernel, 33..256 the prefill kernel
+ *   block_m    1..32 runs the decode kernel (1..16: its 16-row variant), 33..192 the prefill kernel
  *   topk_weights float32 [T, top_k] (COMBINE only, else may be NULL)
  *   c          plain: bf16 [T*top_k, n] at row f; SWIGLU: [T*top_k, n/2]; COMBINE: [T, n] */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, int k, const moe_w4a16_desc* desc,

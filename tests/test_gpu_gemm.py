@@ -60,7 +60,7 @@ def test_indexed_tile_edges(block_m, counts):
     assert_close(gpu, ref, f"edges bm={block_m}")
 
 
-@pytest.mark.parametrize("block_m", [32, 192])
+@pytest.mark.parametrize("block_m", [16, 32, 192])
 def test_indexed_gate_up_mode_and_swiglu(block_m):
     rng = np.random.default_rng(7 + block_m)
     e, t, k, kd, n = 5, 90, 2, 256, 512
@@ -92,7 +92,7 @@ def test_indexed_down_with_combine(block_m):
     assert np.array_equal(gpu, gpu2)
 
 
-@pytest.mark.parametrize("block_m", [32, 64, 192])
+@pytest.mark.parametrize("block_m", [16, 32, 64, 192])
 def test_indexed_sorted_slot_hand_off(block_m):
     """gate_up with OUT_SORTED writes rows at sorted_ids slots; down with A_SORTED reads them there."""
     rng = np.random.default_rng(200 + block_m)
@@ -162,6 +162,29 @@ def test_masked_matches_oracle_expected_m_only_picks_launch(kernel, expected_m, 
     assert M.get_device_error(ws) == 0
     ref, valid = O.masked_gemm(a3, masked_m, lambda x: (qw[x], sc[x]), n)
     assert_close(dev_to_bits(out)[valid], ref[valid], f"masked {kernel} em={expected_m}")
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_masked_budget_of_16_rows(flags, monkeypatch):
+    """A masked budget of at most 16 rows per expert (the 16-row decode variant), counts 0..16."""
+    monkeypatch.setenv("MOE_W4A16_FORCE_KERNEL", "decode")
+    rng = np.random.default_rng(55 + flags)
+    counts = [16, 0, 5, 9, 16, 1, 13, 8, 0, 15, 2, 16]
+    e, kd, n, max_m = len(counts), 320, 512, 16
+    ids = ids_from_counts(rng, counts)
+    t = ids.shape[0]
+    a = random_acts(rng, t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    masked_m, mrows = O.masked_layout(ids, e, max_m)
+    a3 = O.gather_rows(a, mrows.reshape(-1), 1).reshape(e, max_m, kd)
+    pw = prepare_dev(qw, sc, 2 if flags else 1, DEV)
+    ws = M.workspace(M.LAYOUT_MASKED, t, 1, e, n, kd, 0, 0, DEV)
+    out = M.masked(bits_to_dev(a3, DEV), i32_to_dev(masked_m, DEV), 6, pw, ws, flags=flags)
+    assert M.get_device_error(ws) == 0
+    y = O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), n)
+    ref = O.swiglu(y) if flags else y
+    valid = mrows.reshape(-1) >= 0
+    assert_close(dev_to_bits(out)[valid], ref[mrows.reshape(-1)[valid]], f"masked 16-row budget flags={flags}")
 
 
 @pytest.mark.parametrize("kernel", ["decode", "prefill"])

@@ -38,6 +38,9 @@ const DeviceInfo& device_info(int device) {
 // sm_103a the measured crossover of the two families sits lower because the
 // tcgen05 kernel's tile N shrinks to the block's rows (16-row granularity).
 constexpr int kDecodeMaxTokE = 48;
+// Average routed rows per expert up to which decode row blocks hold 16 rows
+// (three CTAs per SM); above it 32 (fewer blocks per loaded expert).
+constexpr int kDecodeSmallTokE = 4;
 
 static bool log_enabled() {
   static const bool on = [] {
@@ -332,7 +335,10 @@ moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_e
   pl.tok_e = static_cast<int32_t>(tok_e > (1 << 30) ? (1 << 30) : tok_e);
   pl.kernel = tok_e < kDecodeMaxTokE ? MOE_W4A16_KERNEL_DECODE : MOE_W4A16_KERNEL_PREFILL;
   if (forced_kernel() != 0) pl.kernel = forced_kernel();
-  pl.block_m = pl.kernel == MOE_W4A16_KERNEL_DECODE ? kDecodeRows : kPrefillRows;
+  if (pl.kernel == MOE_W4A16_KERNEL_DECODE)
+    pl.block_m = tok_e <= kDecodeSmallTokE ? kDecodeRowsSmall : kDecodeRows;
+  else
+    pl.block_m = kPrefillRows;
   const DeviceInfo& di = device_info(device);
   pl.grid = pl.kernel == MOE_W4A16_KERNEL_DECODE ? 2 * di.sm_count : di.sm_count;
   if (log_enabled())

@@ -12,11 +12,13 @@
 //   * eight consumer warps each own 16 channels of both 128-channel chunks of
 //     the unit: a lane's 16-byte load yields four k-steps of A operands, which
 //     are dequantised in registers (dequant_fu: (q - 8) * s, one BF16 rounding)
-//     and fed to mma.m16n8k16 against up to four 8-row token tiles;
+//     and fed to mma.m16n8k16 against up to four (two) 8-row token tiles;
 //   * the stage is released as soon as its bytes are in registers.
 // Work units are (row block <= 32 rows, 256-channel group), assigned to a
 // persistent grid in a fixed interleaved order once the device-side block
 // count is known (a semi-static schedule, the page's 186 us vs 216 us point).
+// Blocks of at most 16 rows run a variant with half the activation stage and
+// accumulators, small enough for three CTAs per SM.
 // Epilogues: BF16 store, SwiGLU (gate and up channels of a unit sit in the
 // same lane), or the top-k combine (routed rows staged in BF16, the last of
 // the top_k arrivals for a (token, channel slice) sums them in slot order).
@@ -31,21 +33,28 @@ namespace decode {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRows = kDecodeRows;                      // 32
 constexpr int kActStride = 144;                         // 128 B of k + 16 B pad (conflict-free ldmatrix)
-constexpr int kActBytes = kRows * kActStride;           // 4608
-constexpr int kStageBytes = 2 * kChunkBytes + kActBytes;  // 13824
 #ifndef MOE_W4A16_DECODE_STAGES
 #define MOE_W4A16_DECODE_STAGES 6
 #endif
 constexpr int kStages = MOE_W4A16_DECODE_STAGES;
-constexpr int kBarOffset = kStages * kStageBytes;
 constexpr int kMiscBytes = 256;
 constexpr int kSlices = kConsumerWarps;                 // combine counter slices per group
 
-__host__ __device__ constexpr int smem_bytes(int prefix_entries) {
-  return kBarOffset + kMiscBytes + prefix_entries * 4;
-}
+// Geometry of the kernel variant whose row blocks hold up to ROWS (16 or 32)
+// routed rows. The 16-row variant's smaller stages and accumulators (72
+// registers) let three CTAs share an SM instead of two, so more warps hide the
+// latency of the dequantisation chains.
+template <int ROWS>
+struct Geo {
+  static constexpr int kTiles = ROWS / 8;                              // 8-row MMA token tiles
+  static constexpr int kActBytes = ROWS * kActStride;
+  static constexpr int kStageBytes = 2 * kChunkBytes + kActBytes;      // 11520 / 13824
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kCtasPerSm = ROWS == 16 ? 3 : 2;
+  static constexpr int kRowIters = ROWS / 4;                           // activation pieces per producer lane
+  static constexpr int smem_bytes(int prefix_entries) { return kBarOffset + kMiscBytes + prefix_entries * 4; }
+};
 
 #ifdef MOE_W4A16_PIPE_STATS
 __device__ unsigned long long g_decode_stats[16];
@@ -70,14 +79,14 @@ __device__ __forceinline__ void store_bf16(uint16_t* base, int64_t idx, float v)
 // stage, a lane loads its four FU words of each chunk, its scales, and the
 // activation B fragments of NT tiles, releases the stage, then dequantises
 // 8 FUs and issues 8*NT MMAs. Returns false when a wait gave up.
-template <int NT>
+template <int ROWS, int NT>
 __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s, int& stage, uint32_t& phase,
-                                             uint32_t wq_off, uint32_t sc_off, int lane, float (&acc)[2][4][4],
-                                             PipeStats& ps) {
+                                             uint32_t wq_off, uint32_t sc_off, int lane,
+                                             float (&acc)[2][Geo<ROWS>::kTiles][4], PipeStats& ps) {
 #pragma unroll
   for (int c = 0; c < 2; ++c)
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < Geo<ROWS>::kTiles; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
   const uint32_t act_lane = 2 * kChunkBytes + (lane & 7) * kActStride + (lane >> 3) * 16;
@@ -86,7 +95,7 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
     if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) return false;
     ps.stop(0);
     ps.add(1, 1);
-    const uint32_t sb = s.stages + stage * kStageBytes;
+    const uint32_t sb = s.stages + stage * Geo<ROWS>::kStageBytes;
     const uint4 wq0 = lds128(sb + wq_off);
     const uint4 wq1 = lds128(sb + kChunkBytes + wq_off);
     const uint2 sc0 = lds64(sb + sc_off);
@@ -129,14 +138,16 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
   return true;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmParams p) {
+template <int ROWS>
+__global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_kernel(const GemmParams p) {
+  using G = Geo<ROWS>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Smem s;
   s.stages = smem_u32(smem);
-  s.full = smem_u32(smem + kBarOffset);
+  s.full = smem_u32(smem + G::kBarOffset);
   s.empty = s.full + kStages * 8;
-  s.abort_flag = reinterpret_cast<volatile int*>(smem + kBarOffset + 2 * kStages * 8);
-  s.prefix = reinterpret_cast<int*>(smem + kBarOffset + kMiscBytes);
+  s.abort_flag = reinterpret_cast<volatile int*>(smem + G::kBarOffset + 2 * kStages * 8);
+  s.prefix = reinterpret_cast<int*>(smem + G::kBarOffset + kMiscBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -147,10 +158,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
     *s.abort_flag = 0;
     fence_mbar_init();
   }
-  if (p.layout == MOE_W4A16_LAYOUT_MASKED && warp == 0) masked_prefix_warp(p, kRows, s.prefix);
+  if (p.layout == MOE_W4A16_LAYOUT_MASKED && warp == 0) masked_prefix_warp(p, ROWS, s.prefix);
   __syncthreads();
 
-  const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED ? p.block_m : kRows;
+  const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED ? p.block_m : ROWS;
   const int nblk = num_row_blocks(p, rows_per_block, s.prefix);
   const int64_t total_units = static_cast<int64_t>(nblk) * p.NG;
 
@@ -172,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
       if (vmask == 0) continue;
       const uint8_t* wsrc = p.chunks + group_offset(e, gp, p.NB, p.KC);
       // activation rows by cp.async: lane copies 16-byte piece (lane & 7) of rows (lane >> 3) + 4j
-      const uint16_t* asrc[8];
+      const uint16_t* asrc[G::kRowIters];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < G::kRowIters; ++j) {
         const int row = (lane >> 3) + 4 * j;
         const int ar = __shfl_sync(0xffffffffu, rr.a_row, row);
         asrc[j] = ar >= 0 ? p.a + static_cast<int64_t>(ar) * p.K + (lane & 7) * 8 : nullptr;
@@ -186,13 +197,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
         pps.stop(0);
         pps.add(1, 1);
         const uint32_t full = s.full + 8 * stage;
-        const uint32_t sb = s.stages + stage * kStageBytes;
+        const uint32_t sb = s.stages + stage * G::kStageBytes;
         if (lane == 0) {
           mbar_arrive_expect_tx(full, kPairBytes);
           bulk_g2s_hint(sb, wsrc + static_cast<size_t>(kc) * kPairBytes, kPairBytes, full, pol);
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < G::kRowIters; ++j)
           if (asrc[j] != nullptr) cp_async16(sb + adst + 4 * j * kActStride, asrc[j] + kc * kChunkK, 16);
         cp_async_arrive_noinc(full);
         issued_any = true;
@@ -236,15 +247,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
       if (vmask == 0) continue;
       const int ntiles = (32 - __clz(vmask) + 7) >> 3;
 
-      float acc[2][4][4];
+      float acc[2][G::kTiles][4];
       bool ok;
       cps.start();
       const long long t_unit = clock64();
       switch (ntiles) {
-        case 1: ok = consume_unit<1>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
-        case 2: ok = consume_unit<2>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
-        case 3: ok = consume_unit<3>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
-        default: ok = consume_unit<4>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
+        case 1: ok = consume_unit<ROWS, 1>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
+        case 2: ok = consume_unit<ROWS, 2>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
+        case 3: ok = consume_unit<ROWS, (G::kTiles > 2 ? 3 : 2)>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps);
+                break;
+        default: ok = consume_unit<ROWS, G::kTiles>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
       }
       cps.add(2, static_cast<unsigned long long>(clock64() - t_unit));
       cps.add(4, 1);
@@ -258,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
         const bool combine = p.flags & MOE_W4A16_FLAG_COMBINE;
         const int chl = warp * 16 + g;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
+        for (int nt = 0; nt < G::kTiles; ++nt) {
           if (nt >= ntiles) break;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -327,31 +339,44 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(const GemmPara
 
 }  // namespace decode
 
-cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
-  using namespace decode;
+namespace decode {
+
+template <int ROWS>
+cudaError_t launch_rows(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
+  using G = Geo<ROWS>;
   const DeviceInfo& di = device_info(device);
   const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
-  const int smem = smem_bytes(prefix_entries);
   static bool attr_set[64] = {false};
   if (device >= 0 && device < 64 && !attr_set[device]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
+    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         G::smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
     if (e != cudaSuccess) return e;
     attr_set[device] = true;
   }
   // upper bound of work units known on the host
   int64_t max_blocks;
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED) max_blocks = p.sorted_cap / p.block_m;
-  else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) max_blocks = p.m_pad / kRows;
-  else max_blocks = static_cast<int64_t>(p.num_experts) * ((p.max_m + kRows - 1) / kRows);
-  int64_t units = max_blocks * p.NG;
-  int64_t grid = static_cast<int64_t>(di.sm_count) * 2;
+  else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) max_blocks = p.m_pad / ROWS;
+  else max_blocks = static_cast<int64_t>(p.num_experts) * ((p.max_m + ROWS - 1) / ROWS);
+  const int64_t units = max_blocks * p.NG;
+  int64_t grid = static_cast<int64_t>(di.sm_count) * G::kCtasPerSm;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  decode_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p);
+  decode_gemm_kernel<ROWS><<<static_cast<int>(grid), kThreads, G::smem_bytes(prefix_entries), stream>>>(p);
   note_launch();
   if (grid_out) *grid_out = static_cast<int>(grid);
   return cudaGetLastError();
+}
+
+}  // namespace decode
+
+// Row blocks of at most 16 rows (indexed block_m <= 16, masked budget <= 16) run
+// the 16-row variant; contiguous blocks and larger ones the 32-row variant.
+cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
+  const bool small = (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.block_m <= kDecodeRowsSmall) ||
+                     (p.layout == MOE_W4A16_LAYOUT_MASKED && p.max_m <= kDecodeRowsSmall);
+  return small ? decode::launch_rows<kDecodeRowsSmall>(p, device, stream, grid_out)
+               : decode::launch_rows<kDecodeRows>(p, device, stream, grid_out);
 }
 
 }  // namespace moe
