@@ -171,7 +171,7 @@ def upload_weights(wl, which: str, mode: int, dev):
 class OurArm:
     """Holds device inputs and runs one step of the hot path for a workload."""
 
-    def __init__(self, wl, layout: str, dev):
+    def __init__(self, wl, layout: str, dev, block_m: int = 0):
         import w4a16_int4_mixture_grouped_gb300 as M
         from w4a16_int4_mixture_grouped_gb300.pipeline import MoEFFN
         self.M, self.wl, self.layout, self.dev = M, wl, layout, dev
@@ -220,8 +220,8 @@ class OurArm:
             self.a = bits_to_dev(self.a_np, dev)
             self.out = torch.empty((out_rows, n), dtype=torch.bfloat16, device=dev)
             sched = M.plan(M.LAYOUT_INDEXED, t, k, e, n, kd)
-            self.block_m = int(sched.block_m)
-            self.kernel_family = "decode" if sched.kernel == M.KERNEL_DECODE else "prefill"
+            self.block_m = int(block_m or sched.block_m)
+            self.kernel_family = "decode" if self.block_m <= 32 else "prefill"
             lay = M.LAYOUT_MASKED if layout == "masked" else M.LAYOUT_INDEXED
             self.ws_small = M.workspace(lay, t, k, e, n, kd, self.block_m, 0, dev)
             gemm_flags = self.flags
@@ -467,6 +467,8 @@ def main(argv=None):
     p.add_argument("--layout", default="", choices=["", "indexed", "masked"],
                    help="override the layout of a single-GEMM workload")
     p.add_argument("--max-m", type=int, default=0, help="masked row budget per expert with --layout masked")
+    p.add_argument("--block-m", type=int, default=0,
+                   help="indexed rows per block of a single-GEMM workload instead of the plan's (schedule sweeps)")
     p.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling cases)")
     p.add_argument("--experts", type=int, default=0, help="override the workload's expert count (profiling cases)")
     args = p.parse_args(argv)
@@ -493,7 +495,7 @@ def main(argv=None):
     torch.cuda.set_device(dev)
     import w4a16_int4_mixture_grouped_gb300 as M
     peaks, peaks_src = load_peaks()
-    arm = OurArm(wl, layout, dev)
+    arm = OurArm(wl, layout, dev, block_m=args.block_m)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
@@ -553,13 +555,17 @@ def main(argv=None):
                 "peak_source": f"{peaks_src} hbm_gbs"}
     roof["algorithmic"] = {"flops": arm.dom_flops, "bytes": arm.dom_bytes}
     # DRAM bytes per launch from the committed ncu capture of this kernel and workload (null if stale or absent)
-    default_wl = args.workload if not (args.tokens or args.experts or args.layout) else None
+    default_wl = args.workload if not (args.tokens or args.experts or args.layout or args.block_m) else None
     roof["traffic"] = recorded_traffic(default_wl) if default_wl else None
+    config = config_of(wl, layout)
+    if getattr(arm, "block_m", None) and layout == "indexed":
+        config["block_m"] = arm.block_m
+        config["kernel"] = arm.kernel_family
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic", "config": config_of(wl, layout),
+        "dtype": "bf16", "data": "synthetic", "config": config,
         "throughput": {"tflops": arm.flops / (ms_per_step * 1e-3) / 1e12,
                        "weight_gbs": arm.weight_bytes / (ms_per_step * 1e-3) / 1e9,
                        "active_experts": arm.e_active},

@@ -7,19 +7,22 @@
 // tensor memory (TMEM), issued by one thread, so the roles become:
 //
 //   warp 0      : allocates TMEM; lane 0 streams the unit's two prepared
-//                 chunks per k-chunk (9 KB) with 1-D bulk copies
-//   warp 1      : lane 0 issues tcgen05.mma (M = 128 channels per tile, two
-//                 tiles per unit, N = the block's rows rounded up to 16, K = 16)
-//   warps 2-3   : gather the block's activation rows (cp.async, 16 B each) into
-//                 a 128-byte-swizzled K-major tile: rows 0-127 / 128-255
-//   warps 4-11  : dequantise (warps 4-7: channel tile 0, warps 8-11: tile 1)
-//                 into a 128-byte-swizzled K-major BF16 tile with stmatrix,
-//                 then run the epilogue from TMEM
+//                 chunks per k-chunk (9 KB) with one 1-D bulk copy
+//   warps 1, 3  : lane 0 issues tcgen05.mma for one 128-channel tile each
+//                 (M = 128, N = the block's rows rounded up to 16, K = 16),
+//                 A operand in TMEM, B in shared memory; one thread issues an
+//                 MMA only every ~100 cycles, so the tiles get a thread each
+//   warp 2      : loads the block's activation rows per k-chunk with TMA into
+//                 a 128-byte-swizzled K-major tile (16-row boxes when the rows
+//                 are consecutive, tile::gather4 otherwise)
+//   warps 4-19  : dequantise one 16-channel m-tile each per k-chunk in
+//                 registers and store it to TMEM as the MMA's A operand
+//                 (tcgen05.st), then run the epilogue from TMEM
 //
 // Operands are "swapped" as in the page's decode design: the dequantised
 // weights are the MMA's M operand and the routed rows its N operand, so a
 // block of r rows costs ceil(r/16)*16 columns, not a 128-row tile. Both
-// accumulators (2 x 256 columns of FP32) live in TMEM; for SwiGLU the gate
+// accumulators (2 x 192 columns of FP32) live in TMEM; for SwiGLU the gate
 // and up tiles of a unit hold matching channels in the same TMEM lane.
 // Every mbarrier wait is bounded (common.cuh); no named barrier is used after
 // the role split, so an abort can never strand a warp.
@@ -40,7 +43,9 @@ __device__ __forceinline__ unsigned long long* pipe_stats_ptr() { return g_pipe_
 __device__ __forceinline__ unsigned long long* pipe_stats_ptr() { return nullptr; }
 #endif
 
-constexpr int kThreads = 384;
+constexpr int kDequantWarps = 16;          // one 16-channel m-tile of the unit each per k-chunk
+constexpr int kIssuers = 2;                // MMA-issuing warps, one per 128-channel tile
+constexpr int kThreads = (4 + kDequantWarps) * 32;
 constexpr int kRows = kPrefillRows;        // 192: rows (MMA N) per block
 #ifndef MOE_W4A16_PREFILL_XSTAGES
 #define MOE_W4A16_PREFILL_XSTAGES 5
@@ -49,7 +54,10 @@ constexpr int kRows = kPrefillRows;        // 192: rows (MMA N) per block
 #define MOE_W4A16_PREFILL_PSTAGES 6
 #endif
 constexpr int kXStages = MOE_W4A16_PREFILL_XSTAGES;   // activation tiles (24 KB each)
-constexpr int kWStages = 2;                           // dequantised weight stages, in TMEM
+#ifndef MOE_W4A16_PREFILL_WSTAGES
+#define MOE_W4A16_PREFILL_WSTAGES 2
+#endif
+constexpr int kWStages = MOE_W4A16_PREFILL_WSTAGES;   // dequantised weight stages, in TMEM
 constexpr int kPStages = MOE_W4A16_PREFILL_PSTAGES;   // packed weight chunks (9 KB each)
 constexpr int kXBytes = kRows * 128;       // 24 KB: 192 rows x 64 k x bf16 (multiple of 1024)
 constexpr int kPBytes = 2 * kChunkBytes;   // 9 KB
@@ -216,19 +224,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(p_full + 8 * i, 1);
-      mbar_init(p_empty + 8 * i, 8);
+      mbar_init(p_empty + 8 * i, kDequantWarps);
     }
     for (int i = 0; i < kXStages; ++i) {
       mbar_init(x_full + 8 * i, 1);
-      mbar_init(x_empty + 8 * i, 1);
+      mbar_init(x_empty + 8 * i, kIssuers);
     }
     for (int i = 0; i < kWStages; ++i) {
-      mbar_init(w_full + 8 * i, 8);
-      mbar_init(w_empty + 8 * i, 1);
+      mbar_init(w_full + 8 * i, kDequantWarps);
+      mbar_init(w_empty + 8 * i, kIssuers);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 8);
-    mbar_init(drain_bar, 1);
+    mbar_init(acc_full, kIssuers);
+    mbar_init(acc_empty, kDequantWarps);
+    mbar_init(drain_bar, kIssuers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -295,9 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(p_full + 8 * st, ph);
       }
     }
-  } else if (warp == 1) {
-    // ----------------------------------------------------- MMA issuer
-    stats_base = 8;
+  } else if (warp == 1 || warp == 3) {
+    // ----------------------------------------------------- MMA issuers (warp 1: tile 0, warp 3: tile 1)
+    // A single thread issues a tcgen05.mma only every ~100 cycles, so each channel tile
+    // has its own issuing warp and accumulator; the consumers' barriers count both.
+    const int mtile = warp == 1 ? 0 : 1;
+    if (warp == 1) stats_base = 8;
     int xs = 0, ws = 0;
     uint32_t xph = 0, wph = 0, aph = 0;
     for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
@@ -331,8 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t bdesc = sw128_desc(xa + ks * 32);
             const uint32_t acc = (kc | ks) != 0;
-            tc_mma_ts(tmem, wa + ks * 8, bdesc, idesc, acc);
-            tc_mma_ts(tmem + kAccCols, wa + kAStageCols / 2 + ks * 8, bdesc, idesc, acc);
+            tc_mma_ts(tmem + mtile * kAccCols, wa + mtile * (kAStageCols / 2) + ks * 8, bdesc, idesc, acc);
           }
           tc_commit(x_empty + 8 * xs);
           tc_commit(w_empty + 8 * ws);
@@ -421,14 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(x_full + 8 * st, ph);
       }
     }
-  } else if (warp == 3) {
-    // spare warp: no role
   } else {
     // ----------------------------------------------------- dequant + epilogue
     PipeStats pst;
-    const int dw = warp - 4;            // 0..7
-    const int tile = dw >> 2;           // channel tile (chunk) of the unit
-    const int wq = dw & 3;              // m-tiles 2wq, 2wq+1 of the tile; TMEM lane quarter
+    const int dw = warp - 4;            // 0..15
+    const int wq = dw & 3;              // TMEM lane quarter (warp % 4, the lanes this warp may access)
+    const int tile = (dw >> 2) & 1;     // channel tile (chunk) of the unit
+    const int mj = dw >> 3;             // m-tile 2wq + mj of the tile = TMEM lanes 32wq + 16mj .. +15
     const int g = lane >> 2;
     int ps = 0, ws = 0;
     uint32_t pph = 0, wph = 0, aph = 0;
@@ -448,13 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(p_full + 8 * ps, pph, abort_flag, p.err)) goto d_done;
         pst.stop(0);
         const uint32_t pa = sbase + kPOff + ps * kPBytes + tile * kChunkBytes;
-        uint4 wv[2];
-        uint2 sv[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          wv[j] = lds128(pa + ((2 * wq + j) * 32 + lane) * 16);
-          sv[j] = lds64(pa + kChunkWBytes + ((2 * wq + j) * 8 + g) * 8);
-        }
+        const int mt = 2 * wq + mj;
+        const uint4 wv = lds128(pa + (mt * 32 + lane) * 16);
+        const uint2 sv = lds64(pa + kChunkWBytes + (mt * 8 + g) * 8);
         __syncwarp();
         if (lane == 0) mbar_arrive(p_empty + 8 * ps);
         if (++ps == kPStages) {
@@ -467,12 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         pst.start();
         // A operand of this tile: TMEM lanes = channels, columns = k pairs of the 64-k chunk
         const uint32_t at = tmem + kACol0 + ws * kAStageCols + tile * (kAStageCols / 2);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint32_t w4[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+        {
+          const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
           uint32_t sg[2], sg8[2];
-          scale_pairs(sv[j], 0, sg[0], sg8[0]);
-          scale_pairs(sv[j], 1, sg[1], sg8[1]);
+          scale_pairs(sv, 0, sg[0], sg8[0]);
+          scale_pairs(sv, 1, sg[1], sg8[1]);
           uint32_t frag[16];
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
@@ -483,8 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             frag[4 * ks + 2] = a[2];
             frag[4 * ks + 3] = a[3];
           }
-          // m-tile 2wq + j = TMEM lanes 32wq + 16j .. +15 (this warp's lane quarter)
-          tmem_st_16x128b_x8(at + (static_cast<uint32_t>(32 * wq + 16 * j) << 16), frag);
+          tmem_st_16x128b_x8(at + (static_cast<uint32_t>(32 * wq + 16 * mj) << 16), frag);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -507,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int q = wq;  // TMEM lanes 32q..32q+31 = channels 32q+lane of each tile
         const int nchunks = nr >> 4;
-        for (int cc = tile; cc < nchunks; cc += 2) {
+        for (int cc = tile + 2 * mj; cc < nchunks; cc += 4) {
           uint32_t d0[16], d1[16];
           const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + cc * 16;
           tmem_ld16(taddr, d0);

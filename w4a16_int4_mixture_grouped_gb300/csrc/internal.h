@@ -116,7 +116,10 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
 // Rows per block the kernels use for the contiguous / masked layouts.
 constexpr int kDecodeRows = 32;
 constexpr int kDecodeRowsSmall = 16;   // decode blocks this small run three CTAs per SM
-constexpr int kPrefillRows = 192;   // two 128-channel accumulators of 192 columns + weight stages fill TMEM
+#ifndef MOE_W4A16_PREFILL_ROWS
+#define MOE_W4A16_PREFILL_ROWS 192
+#endif
+constexpr int kPrefillRows = MOE_W4A16_PREFILL_ROWS;   // two 128-channel accumulators of 192 columns + weight stages fill TMEM
 constexpr int kContigSeg = 128;
 
 }  // namespace moe
