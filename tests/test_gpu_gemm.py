@@ -282,3 +282,15 @@ def test_mode_mismatch_fails_before_launch():
         M.masked(a3, mm, 1, pw, ws, flags=M.FLAG_SWIGLU)
     assert ei.value.name == "ERR_MODE_MISMATCH"
     assert M.launch_count() == before
+
+
+@pytest.mark.parametrize("tokens,kernel,block_m", [(16, 1, 16), (128, 1, 16), (192, 1, 32), (512, 1, 32),
+                                                   (1536, 2, 192), (8192, 2, 192)])
+def test_plan_picks_family_and_block_from_rows_per_expert(tokens, kernel, block_m):
+    """tok_e = T*top_k/E (384 experts, top-8): decode 16-row blocks up to 4 rows per expert,
+    decode 32-row blocks below 24, the tcgen05 family from 24 rows per expert on."""
+    s = M.plan(M.LAYOUT_INDEXED, tokens, 8, 384, 4096, 7168)
+    assert (s.kernel, s.block_m) == (kernel, block_m)
+    assert s.tok_e == -(-tokens * 8 // 384)
+    m = M.plan(M.LAYOUT_MASKED, tokens, 8, 384, 4096, 7168, expected_m=s.tok_e)
+    assert m.kernel == kernel

@@ -35,9 +35,11 @@ const DeviceInfo& device_info(int device) {
 
 // Routed rows per expert below which the decode (warp-MMA) family runs.
 // The Chord page puts its block-M switch near 80 routed tokens per expert; on
-// sm_103a the measured crossover of the two families sits lower because the
-// tcgen05 kernel's tile N shrinks to the block's rows (16-row granularity).
-constexpr int kDecodeMaxTokE = 48;
+// sm_103a the measured crossover sits lower: at K=7168, N=4096 the decode
+// family is faster at 11 rows per expert (1.49 vs 2.12 ms) and the tcgen05
+// family at 32 (2.15 vs 2.92 ms), where 32-row decode blocks start to split
+// experts and stream their weights twice.
+constexpr int kDecodeMaxTokE = 24;
 // Average routed rows per expert up to which decode row blocks hold 16 rows
 // (three CTAs per SM); above it 32 (fewer blocks per loaded expert).
 constexpr int kDecodeSmallTokE = 4;
