@@ -284,7 +284,7 @@ def test_mode_mismatch_fails_before_launch():
     assert M.launch_count() == before
 
 
-@pytest.mark.parametrize("tokens,kernel,block_m", [(16, 1, 16), (128, 1, 16), (192, 1, 32), (512, 1, 32),
+@pytest.mark.parametrize("tokens,kernel,block_m", [(16, 1, 16), (128, 1, 16), (192, 1, 16), (256, 1, 32), (512, 1, 32),
                                                    (1536, 2, 192), (8192, 2, 192)])
 def test_plan_picks_family_and_block_from_rows_per_expert(tokens, kernel, block_m):
     """tok_e = T*top_k/E (384 experts, top-8): decode 16-row blocks up to 4 rows per expert,
