@@ -29,9 +29,11 @@
  *     kernel gives up after about two seconds and records
  *     MOE_W4A16_ERR_DEVICE_TIMEOUT instead of hanging.
  *   - `ws` is a caller-owned workspace of at least moe_w4a16_workspace_size()
- *     bytes (always >= 256: its first bytes hold the device error word). Zero
- *     it once after allocation (moe_w4a16_workspace_init). Calls that share a
- *     workspace must be ordered on one stream.
+ *     bytes (always >= 256: its first bytes hold the device error word and the
+ *     decode kernel's unit hand-out counters). Zero it once after allocation
+ *     (moe_w4a16_workspace_init); every call leaves its counters at zero, but a
+ *     call that recorded a device error may not, so zero it again after one.
+ *     Calls that share a workspace must be ordered on one stream.
  */
 #ifndef MOE_W4A16_H_
 #define MOE_W4A16_H_

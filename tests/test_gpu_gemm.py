@@ -243,8 +243,9 @@ def test_empty_routing_is_a_no_op():
     assert out.shape == (0, 256)
     masked_m = torch.zeros(4, dtype=torch.int32, device=DEV)
     a3 = torch.zeros((4, 16, 128), dtype=torch.bfloat16, device=DEV)
-    M.masked(a3, masked_m, 1, pw, ws)
-    assert M.get_device_error(ws) == 0
+    wsm = M.workspace(M.LAYOUT_MASKED, 1, 1, 4, 256, 128, 0, 0, DEV)
+    M.masked(a3, masked_m, 1, pw, wsm)
+    assert M.get_device_error(ws) == 0 and M.get_device_error(wsm) == 0
 
 
 def test_device_index_checks_do_not_fault():
@@ -255,9 +256,9 @@ def test_device_index_checks_do_not_fault():
     a = bits_to_dev(random_acts(rng, 8, 128), DEV)
     # masked_m above the budget -> capacity error, no out-of-bounds access
     a3 = torch.zeros((4, 16, 128), dtype=torch.bfloat16, device=DEV)
-    M.masked(a3, i32_to_dev(np.array([3, 40, 0, 1]), DEV), 4, pw, ws)
-    assert M.get_device_error(ws) == 5
-    M.clear_device_error(ws)
+    wsm = M.workspace(M.LAYOUT_MASKED, 8, 1, 4, 256, 128, 0, 0, DEV)
+    M.masked(a3, i32_to_dev(np.array([3, 40, 0, 1]), DEV), 4, pw, wsm)
+    assert M.get_device_error(wsm) == 5
     # sorted_ids holding an id past the sentinel and an expert id out of range
     s_ids = i32_to_dev(np.array([0, 1, 99, 8] + [8] * 28), DEV)
     e_ids = i32_to_dev(np.array([7]), DEV)
@@ -268,6 +269,15 @@ def test_device_index_checks_do_not_fault():
     e_ids = i32_to_dev(np.array([1]), DEV)
     M.indexed(a, pw, s_ids, e_ids, npp, 8, 1, 32, ws)
     assert M.get_device_error(ws) == 8
+    # the same checks on 16-row blocks (the one-CTA-per-SM decode kernel)
+    ws16 = M.workspace(M.LAYOUT_INDEXED, 8, 1, 4, 256, 128, 16, 0, DEV)
+    s16 = i32_to_dev(np.array([0, 1, 99, 8] + [8] * 12), DEV)
+    npp16 = i32_to_dev(np.array([16]), DEV)
+    M.indexed(a, pw, s16, i32_to_dev(np.array([7]), DEV), npp16, 8, 1, 16, ws16)
+    assert M.get_device_error(ws16) == 8
+    M.clear_device_error(ws16)
+    M.indexed(a, pw, s16, i32_to_dev(np.array([1]), DEV), npp16, 8, 1, 16, ws16)
+    assert M.get_device_error(ws16) == 8
 
 
 def test_mode_mismatch_fails_before_launch():

@@ -180,6 +180,8 @@ moe_w4a16_status moe_w4a16_align_size(int num_tokens, int top_k, int num_experts
 }
 
 // Workspace of a GEMM call: [header 256 B][gathered activations][combine counters][combine staging].
+// Header: int32 0 = device error word; int32 16, 17 = the decode kernel's unit hand-out counters.
+constexpr int kGrabWord = 16;
 struct WsLayout {
   size_t gather_off = 0, gather_bytes = 0;
   size_t counters_off = 0, counters_bytes = 0;
@@ -441,6 +443,7 @@ static void fill_common(GemmParams& p, const moe_w4a16_desc* desc, const void* p
   p.c = c;
   p.c_cols = (flags & MOE_W4A16_FLAG_SWIGLU) ? p.N / 2 : p.N;
   p.err = static_cast<int*>(ws);
+  p.grab = static_cast<int*>(ws) + kGrabWord;
   if (flags & MOE_W4A16_FLAG_COMBINE) {
     p.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + L.counters_off);
     p.y_ws = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.y_off);

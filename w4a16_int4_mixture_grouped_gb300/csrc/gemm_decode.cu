@@ -14,11 +14,17 @@
 //     are dequantised in registers (dequant_fu: (q - 8) * s, one BF16 rounding)
 //     and fed to mma.m16n8k16 against up to four (two) 8-row token tiles;
 //   * the stage is released as soon as its bytes are in registers.
-// Work units are (row block <= 32 rows, 256-channel group), assigned to a
-// persistent grid in a fixed interleaved order once the device-side block
-// count is known (a semi-static schedule, the page's 186 us vs 216 us point).
-// Blocks of at most 16 rows run a variant with half the activation stage and
-// accumulators, small enough for three CTAs per SM.
+// Work units are (row block <= 32 rows, 256-channel group) in a fixed order
+// (the groups of a block, then the next block), known once the device-side
+// block count is. Each CTA's producer takes the next unit from a counter when
+// its ring has room and marks the unit's first stage for its consumers. The
+// page prefers a semi-static schedule to a dynamic one (186 us vs 216 us); on
+// sm_103a with two or three CTAs per SM the warp schedulers favour the oldest
+// CTA, so CTAs given equal static shares finish far apart, while units handed
+// out on demand keep every SM busy to the end (measured: down+combine
+// 655 -> 601 us, gate_up at 128 tokens 1185 -> 1121 us). Blocks of at most 16
+// rows run a variant with half the activation stage and accumulators, small
+// enough for three CTAs per SM.
 // Epilogues: BF16 store, SwiGLU (gate and up channels of a unit sit in the
 // same lane), or the top-k combine (routed rows staged in BF16, the last of
 // the top_k arrivals for a (token, channel slice) sums them in slot order).
@@ -38,7 +44,9 @@ constexpr int kActStride = 144;                         // 128 B of k + 16 B pad
 #define MOE_W4A16_DECODE_STAGES 6
 #endif
 constexpr int kStages = MOE_W4A16_DECODE_STAGES;
-constexpr int kMiscBytes = 256;
+constexpr int kMiscBytes = 256;                         // barriers, abort flag, stage descriptors
+constexpr int kDescOffset = 160;                        // int per stage inside the misc area
+static_assert(2 * kStages * 8 + 4 <= kDescOffset && kDescOffset + 4 * kStages <= kMiscBytes, "misc area layout");
 constexpr int kSlices = kConsumerWarps;                 // combine counter slices per group
 
 // Geometry of the kernel variant whose row blocks hold up to ROWS (16 or 32)
@@ -148,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
   s.empty = s.full + kStages * 8;
   s.abort_flag = reinterpret_cast<volatile int*>(smem + G::kBarOffset + 2 * kStages * 8);
   s.prefix = reinterpret_cast<int*>(smem + G::kBarOffset + kMiscBytes);
+  // unit of the piece that starts at each stage (-1: no more work), written by the producer
+  volatile int* desc = reinterpret_cast<volatile int*>(smem + G::kBarOffset + kDescOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -172,7 +182,12 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     uint32_t phase = 0;
     bool issued_any = false;
     PipeStats pps;
-    for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+    while (true) {
+      // units are handed out in order, one at a time, to whichever CTA asks next
+      int64_t u = 0;
+      if (lane == 0) u = atomicAdd(p.grab, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u >= total_units) break;
       const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
       int local;
       const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
@@ -199,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
         const uint32_t full = s.full + 8 * stage;
         const uint32_t sb = s.stages + stage * G::kStageBytes;
         if (lane == 0) {
+          if (kc == 0) desc[stage] = static_cast<int>(u);
           mbar_arrive_expect_tx(full, kPairBytes);
           bulk_g2s_hint(sb, wsrc + static_cast<size_t>(kc) * kPairBytes, kPairBytes, full, pol);
         }
@@ -212,6 +228,15 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
           phase ^= 1u;
         }
       }
+    }
+    // no more units: one stage carries the end mark (33 plain arrivals complete its phase)
+    if (warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err)) {
+      if (lane == 0) {
+        desc[stage] = -1;
+        mbar_arrive(s.full + 8 * stage);
+      }
+      __syncwarp();
+      mbar_arrive(s.full + 8 * stage);
     }
   producer_done:
     cp_async_wait<0>();
@@ -236,15 +261,19 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     const uint32_t wq_off = (warp * 32 + lane) * 16;
     const uint32_t sc_off = kChunkWBytes + (warp * 8 + g) * 8;
     PipeStats cps;
-    for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+    while (true) {
       cps.stop(3);   // epilogue of the previous unit (and unit bookkeeping)
+      // the next unit is the one the producer put at the head of the current stage
+      if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) goto consumer_done;
+      const int u = desc[stage];
+      if (u < 0) break;
       const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
       int local;
       const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
-      if (e < 0) continue;
+      if (e < 0) break;   // never: the producer hands out only units with work
       const RowRef rr = block_row(p, blk, e, local, rows_per_block, lane);
       const unsigned vmask = __ballot_sync(0xffffffffu, rr.a_row >= 0);
-      if (vmask == 0) continue;
+      if (vmask == 0) break;
       const int ntiles = (32 - __clz(vmask) + 7) >> 3;
 
       float acc[2][G::kTiles][4];
@@ -334,6 +363,16 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     }
   consumer_done:
     if (lane == 0) cps.flush(decode_stats_ptr() + 8);
+  }
+  // the last CTA out zeroes the hand-out counters for the next call
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.grab + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      p.grab[0] = 0;
+      p.grab[1] = 0;
+      __threadfence();
+    }
   }
 }
 

@@ -80,6 +80,7 @@ struct GemmParams {
   int num_tokens, top_k;
   uint16_t* y_ws;            // bf16 [R, N] staging
   int* counters;             // [num_tokens, NG]
+  int* grab;                 // decode: [0] next unit to hand out, [1] CTAs done (zero between calls)
 
   // output
   uint16_t* c;
