@@ -91,6 +91,10 @@ def test_workspace_size(lib):
     assert f(0, 8192, 8, 384, 7168, 2048, 256, 2 | 8, ctypes.byref(out)) == 0
     counters = -(-(8192 * 28 * 8 * 4) // 256) * 256
     assert out.value == 256 + counters + 65536 * 7168 * 2
+    # contiguous: + one int4 per 128-row segment of the largest align-built layout, plus the count
+    segs = -(-(8192 * 8 + 384 * 127) // 128)
+    assert f(1, 8192, 8, 384, 4096, 7168, 0, 0, ctypes.byref(out)) == 0
+    assert out.value == 256 + -(-((segs + 1) * 16) // 256) * 256
     assert f(5, 1, 1, 4, 256, 64, 0, 0, ctypes.byref(out)) == 1    # unknown layout
 
 

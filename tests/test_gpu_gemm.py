@@ -143,6 +143,32 @@ def test_contiguous_matches_oracle_and_ignores_poisoned_padding(kernel, monkeypa
     assert np.all(gpu[~valid] == sentinel), "padding rows were written"
 
 
+def test_contiguous_runs_of_segments_on_the_tcgen05_kernel(monkeypatch):
+    """Each expert's run of 128-row segments is taken in blocks of up to 192 rows: counts around
+    the 128 / 192 / 256 / 384 edges, poisoned padding, padding rows left unwritten."""
+    monkeypatch.setenv("MOE_W4A16_FORCE_KERNEL", "prefill")
+    rng = np.random.default_rng(43)
+    counts = [0, 1, 127, 128, 129, 191, 192, 193, 300, 385]
+    e, kd, n = len(counts), 192, 256
+    ids = ids_from_counts(rng, counts)
+    t = ids.shape[0]
+    a = random_acts(rng, t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    row_ids, m_idx = O.contiguous_layout(ids, e)
+    a_pad = O.gather_rows(a, row_ids, 1)
+    a_pad[row_ids < 0] = 0x7FC0
+    pw = prepare_dev(qw, sc, 1, DEV)
+    ws = M.workspace(M.LAYOUT_CONTIGUOUS, t, 1, e, n, kd, 0, 0, DEV)
+    out = torch.full((a_pad.shape[0], n), 12345.0, dtype=torch.bfloat16, device=DEV)
+    M.contiguous(bits_to_dev(a_pad, DEV), i32_to_dev(m_idx, DEV), pw, ws, out=out)
+    assert M.get_device_error(ws) == 0
+    gpu = dev_to_bits(out)
+    ref, valid = O.contiguous_gemm(a_pad, m_idx, lambda x: (qw[x], sc[x]), n)
+    assert_close(gpu[valid], ref[valid], "contiguous runs of segments")
+    sentinel = dev_to_bits(torch.full((1,), 12345.0, dtype=torch.bfloat16))[0]
+    assert np.all(gpu[~valid] == sentinel), "padding rows were written"
+
+
 @pytest.mark.parametrize("kernel", ["decode", "prefill"])
 @pytest.mark.parametrize("expected_m", [1, 40, 1000])
 def test_masked_matches_oracle_expected_m_only_picks_launch(kernel, expected_m, monkeypatch):

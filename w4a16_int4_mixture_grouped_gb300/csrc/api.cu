@@ -179,13 +179,16 @@ moe_w4a16_status moe_w4a16_align_size(int num_tokens, int top_k, int num_experts
   return MOE_W4A16_OK;
 }
 
-// Workspace of a GEMM call: [header 256 B][gathered activations][combine counters][combine staging].
+// Workspace of a GEMM call: [header 256 B][gathered activations][combine counters][combine staging]
+// [contiguous: merged row-block table].
 // Header: int32 0 = device error word; int32 16, 17 = the decode kernel's unit hand-out counters.
 constexpr int kGrabWord = 16;
 struct WsLayout {
   size_t gather_off = 0, gather_bytes = 0;
   size_t counters_off = 0, counters_bytes = 0;
   size_t y_off = 0, y_bytes = 0;
+  size_t cb_off = 0;
+  int cb_segs = 0;   // contiguous: segments the merged block table holds
   size_t total = 0;
 };
 
@@ -215,6 +218,16 @@ static moe_w4a16_status ws_layout(int layout, int num_tokens, int top_k, int num
     L->y_off = off;
     L->y_bytes = align_up(static_cast<size_t>(num_tokens) * top_k * n * sizeof(uint16_t), 256);
     off += L->y_bytes;
+  }
+  if (layout == MOE_W4A16_LAYOUT_CONTIGUOUS) {
+    // one int4 per 128-row segment of the largest contiguous layout align can build, plus the count
+    size_t ms, mb;
+    moe_w4a16_status st = moe_w4a16_align_size(num_tokens, top_k, num_experts, kContigSeg, &ms, &mb);
+    if (st != MOE_W4A16_OK) return st;
+    const size_t segs = ms / kContigSeg;
+    L->cb_segs = static_cast<int>(segs < static_cast<size_t>(kMaxContigSegs) ? segs : kMaxContigSegs);
+    L->cb_off = off;
+    off += align_up((static_cast<size_t>(L->cb_segs) + 1) * 16, 256);
   }
   L->total = off;
   return MOE_W4A16_OK;
@@ -543,7 +556,18 @@ moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad, int k, const
   p.m_pad = m_pad;
   p.row_ids = row_ids;
   p.c_rows = m_pad;
-  return run_gemm(p, pl.kernel, num_tokens, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the table's room: what the caller's workspace holds past the other regions (sized for
+  // the largest layout of the workspace's own call shape, which may exceed this call's)
+  const size_t cb_room = ws_bytes > L.cb_off ? (ws_bytes - L.cb_off) / 16 : 0;
+  if (pl.kernel == MOE_W4A16_KERNEL_PREFILL && m_pad / kContigSeg <= kMaxContigSegs &&
+      static_cast<size_t>(m_pad / kContigSeg) + 1 <= cb_room) {
+    // the tcgen05 kernel takes each expert's run of segments in blocks of up to 192 rows
+    int4* table = reinterpret_cast<int4*>(static_cast<uint8_t*>(ws) + L.cb_off);
+    MOE_CUDA_TRY(launch_contig_blocks(m_indices, m_pad, table, s));
+    p.cblocks = table;
+  }
+  return run_gemm(p, pl.kernel, num_tokens, s);
 }
 
 moe_w4a16_status moe_w4a16_masked(const uint16_t* a3, int num_experts, int max_m, int k, const int32_t* masked_m,

@@ -247,9 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED    ? p.block_m
-                             : p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS ? kContigSeg
-                                                                        : kRows;
+  const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED      ? p.block_m
+                             : p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS
+                                 ? (p.cblocks != nullptr ? kRows : kContigSeg)
+                                 : kRows;
   const int nblk = num_row_blocks(p, rows_per_block, prefix);
   const int64_t total_units = static_cast<int64_t>(nblk) * p.NG;
   PipeStats ps;

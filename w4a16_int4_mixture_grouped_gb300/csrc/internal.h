@@ -70,6 +70,8 @@ struct GemmParams {
   const int32_t* m_indices;
   int m_pad;
 
+  const int4* cblocks;       // contiguous on the tcgen05 kernel: merged row blocks (null: 128-row segments)
+
   // masked
   const int32_t* masked_m;
   int max_m;
@@ -106,6 +108,10 @@ cudaError_t launch_gather_sorted(const uint16_t* src, int64_t src_rows, int K, c
                                  const int32_t* num_post_padded, int64_t sorted_cap, int R, int row_div, uint16_t* dst,
                                  int* err, cudaStream_t stream);
 
+// Row blocks of a contiguous layout for the tcgen05 kernel (see layout.cu): table[0].x = count,
+// table[1 + b] = {first row, expert, rows, 0}; at most kMaxContigSegs segments (else an error).
+cudaError_t launch_contig_blocks(const int32_t* m_indices, int m_pad, int4* table, cudaStream_t stream);
+
 // out[t, :] = bf16(sum_j w[t, j] * y[t*top_k + j, :]), j ascending, FP32 sums.
 cudaError_t launch_combine_rows(const uint16_t* y, const float* w, int T, int top_k, int N, uint16_t* out,
                                 cudaStream_t stream);
@@ -122,5 +128,6 @@ constexpr int kDecodeRowsSmall = 16;   // decode blocks this small run three CTA
 #endif
 constexpr int kPrefillRows = MOE_W4A16_PREFILL_ROWS;   // two 128-channel accumulators of 192 columns + weight stages fill TMEM
 constexpr int kContigSeg = 128;
+constexpr int kMaxContigSegs = 2048;   // merged contiguous blocks: at most 2048 segments (262144 rows)
 
 }  // namespace moe

@@ -122,6 +122,65 @@ __global__ void contiguous_layout_kernel(const int32_t* __restrict__ sorted_ids,
   }
 }
 
+// Row blocks of the contiguous layout for the tcgen05 kernel: each expert's run of
+// 128-row segments is cut into blocks of up to kPrefillRows rows from the run's start,
+// so an expert with up to kPrefillRows rows streams its weights once instead of once per
+// segment. table[0].x = block count; table[1 + b] = {first row, expert, rows, 0}.
+// One CTA of 1024 threads; at most kMaxContigSegs segments (two per thread).
+__global__ void __launch_bounds__(1024) contig_blocks_kernel(const int32_t* __restrict__ m_indices, int nseg,
+                                                               int4* __restrict__ table) {
+  __shared__ int seg_e[kMaxContigSegs];
+  __shared__ int warp_sum[32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int sg = t; sg < nseg; sg += blockDim.x) seg_e[sg] = m_indices[static_cast<int64_t>(sg) * kContigSeg];
+  __syncthreads();
+  // the (up to two) segments of this thread: run starts, run ends and block counts
+  int start[2] = {-1, -1}, end[2] = {0, 0}, nb[2] = {0, 0};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int sg = 2 * t + j;
+    if (sg >= nseg) continue;
+    const int e = seg_e[sg];
+    if (e < 0 || (sg > 0 && seg_e[sg - 1] == e)) continue;
+    int en = sg + 1;
+    while (en < nseg && seg_e[en] == e) ++en;
+    start[j] = sg;
+    end[j] = en;
+    nb[j] = ((en - sg) * kContigSeg + kPrefillRows - 1) / kPrefillRows;
+  }
+  // exclusive prefix of the block counts over threads (segment order)
+  const int mine = nb[0] + nb[1];
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < static_cast<int>(blockDim.x >> 5) ? warp_sum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_sum[lane] = w;   // inclusive over warps
+  }
+  __syncthreads();
+  int off = (warp > 0 ? warp_sum[warp - 1] : 0) + incl - mine;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    for (int b = 0; b < nb[j]; ++b) {
+      const int row0 = start[j] * kContigSeg + b * kPrefillRows;
+      const int rows = min(kPrefillRows, end[j] * kContigSeg - row0);
+      table[1 + off + b] = make_int4(row0, seg_e[start[j]], rows, 0);
+    }
+    off += nb[j];
+  }
+  if (t == blockDim.x - 1) table[0] = make_int4(off, 0, 0, 0);
+}
+
 __global__ void gather_rows_kernel(const uint4* __restrict__ src, int src_rows, int KV,
                                    const int32_t* __restrict__ row_ids, int num_rows, int div, uint4* __restrict__ dst,
                                    int* err) {
@@ -249,6 +308,14 @@ cudaError_t launch_contiguous_layout(const int32_t* sorted_ids, const int32_t* e
   blocks = blocks < 1 ? 1 : (blocks > 4096 ? 4096 : blocks);
   contiguous_layout_kernel<<<blocks, threads, 0, stream>>>(sorted_ids, expert_ids, num_post_padded, R, m_pad,
                                                            m_indices, row_ids);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_contig_blocks(const int32_t* m_indices, int m_pad, int4* table, cudaStream_t stream) {
+  const int nseg = m_pad / kContigSeg;
+  if (nseg > kMaxContigSegs) return cudaErrorInvalidValue;
+  contig_blocks_kernel<<<1, 1024, 0, stream>>>(m_indices, nseg, table);
   note_launch();
   return cudaGetLastError();
 }

@@ -7,7 +7,9 @@
 //                valid when < R (the sentinel); A row = id / a_div; output row = id
 //   contiguous : rows [b*rows, (b+1)*rows) of the padded activations; the
 //                block's expert is m_indices of its first row (-1: no work);
-//                padding rows (m_indices = -1) are invalid
+//                padding rows (m_indices = -1) are invalid. With a merged
+//                block table (tcgen05 kernel) block b is instead {first row,
+//                expert, rows} of the table: up to 192 rows of one expert
 //   masked     : expert e's rows [j*rows, (j+1)*rows) below min(masked_m[e], max_m);
 //                blocks are numbered through a per-CTA prefix over experts
 // Every index read from the caller's arrays is range-checked; a bad value is
@@ -60,7 +62,16 @@ __device__ __forceinline__ int num_row_blocks(const GemmParams& p, int rows, con
     }
     return npp / p.block_m;
   }
-  if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) return p.m_pad / rows;
+  if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) {
+    if (p.cblocks == nullptr) return p.m_pad / rows;
+    const int nb = p.cblocks[0].x;
+    const int cap = p.m_pad / kContigSeg;   // a run of s segments gives at most s blocks
+    if (nb < 0 || nb > cap) {
+      set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
+      return nb < 0 ? 0 : cap;
+    }
+    return nb;
+  }
   return prefix[p.num_experts];
 }
 
@@ -71,7 +82,7 @@ __device__ __forceinline__ int block_expert(const GemmParams& p, int blk, int ro
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED) {
     e = p.expert_ids[blk];
   } else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) {
-    e = p.m_indices[static_cast<int64_t>(blk) * rows];
+    e = p.cblocks != nullptr ? p.cblocks[1 + blk].y : p.m_indices[static_cast<int64_t>(blk) * rows];
     if (e < 0) return -1;
   } else {
     int lo = 0, hi = p.num_experts;  // largest e with prefix[e] <= blk
@@ -116,8 +127,13 @@ __device__ __forceinline__ RowRef block_row(const GemmParams& p, int blk, int e,
     r.out_row = p.out_sorted ? slot : id;
     r.flat = id;
   } else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) {
-    const int row = blk * rows + i;
-    if (row >= p.m_pad) return r;
+    int row = blk * rows + i;
+    if (p.cblocks != nullptr) {
+      const int4 b = p.cblocks[1 + blk];
+      if (i >= b.z) return r;
+      row = b.x + i;
+    }
+    if (row < 0 || row >= p.m_pad) return r;
     const int m = p.m_indices[row];
     if (m < 0) return r;
     if (m != e) {
