@@ -1,6 +1,7 @@
 // Routing -> layout kernels (the Chord page, Figure 3): the indexed align
 // step (sorted_ids with padding sentinels), the masked row lists, the
 // contiguous m_indices, and the row gather that builds padded activations.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -8,30 +9,40 @@
 
 namespace moe {
 
-constexpr int kAlignWarps = 16;
+constexpr int kAlignCtas = 8;    // one thread-block cluster
+constexpr int kAlignWarps = 32;  // warps per CTA
 
-// One CTA. Three passes over the flat routed rows f = t*top_k + j:
-//  A. per-warp histograms of experts over contiguous segments of f;
-//  B. per-expert start offsets (padded to block_m, or e*max_m when masked)
-//     plus per-(warp, expert) offsets = rows of earlier warps;
-//  C. each warp walks its segment in order, ranking equal experts within a
+// One cluster of kAlignCtas CTAs; CTA r takes a contiguous segment of the flat
+// routed rows f = t*top_k + j, split again over its warps:
+//  A. per-warp histograms of experts over the warp's rows (shared memory);
+//  B. per-(warp, expert) offsets within the CTA and the CTA's expert totals;
+//     every CTA then reads the other CTAs' totals through distributed shared
+//     memory: rows of each expert in earlier CTAs, and the expert totals;
+//  C. per-expert start offsets (padded to block_m, or e*max_m when masked);
+//  D. each warp walks its rows in order, ranking equal experts within a
 //     32-row step with match.any, so rows land in ascending f per expert.
-__global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(const int32_t* __restrict__ ids, int R, int E,
-                                                                 int block_m, int max_m,
-                                                                 int32_t* __restrict__ sorted_ids,
-                                                                 int32_t* __restrict__ expert_ids,
-                                                                 int32_t* __restrict__ npp, int32_t* __restrict__ counts,
-                                                                 int32_t* __restrict__ masked_rows, int* err) {
+// No global scratch: the cross-CTA exchange stays on chip.
+__global__ void __cluster_dims__(kAlignCtas, 1, 1) __launch_bounds__(kAlignWarps * 32)
+    align_kernel(const int32_t* __restrict__ ids, int R, int E, int block_m, int max_m,
+                 int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids, int32_t* __restrict__ npp,
+                 int32_t* __restrict__ counts, int32_t* __restrict__ masked_rows, int* err) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
   extern __shared__ int smem[];
-  int* hist = smem;                     // [W][E]
-  int* cnt = hist + kAlignWarps * E;    // [E]
-  int* start = cnt + E;                 // [E + 1]
+  int* hist = smem;                      // [W][E] per-warp counts, then offsets within this CTA
+  int* cta_cnt = hist + kAlignWarps * E; // [E] rows of each expert in this CTA
+  int* before = cta_cnt + E;             // [E] rows of each expert in earlier CTAs
+  int* tot = before + E;                 // [E] rows of each expert
+  int* start = tot + E;                  // [E + 1] padded start of each expert
   const bool masked = max_m > 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  const int seg = (R + kAlignWarps - 1) / kAlignWarps;
-  const int beg = min(R, warp * seg), end = min(R, beg + seg);
+  const int cseg = (R + kAlignCtas - 1) / kAlignCtas;
+  const int cbeg = min(R, rank * cseg), cend = min(R, cbeg + cseg);
+  const int wseg = (cend - cbeg + kAlignWarps - 1) / kAlignWarps;
+  const int beg = min(cend, cbeg + warp * wseg), end = min(cend, beg + wseg);
   for (int i = beg + lane; i < end; i += 32) {
     const int e = ids[i];
     if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
@@ -45,17 +56,30 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(const int32_t* 
       hist[w * E + e] = c;
       c += h;
     }
-    cnt[e] = c;
-    if (counts != nullptr) counts[e] = c;
-    if (masked && c > max_m) set_error(err, MOE_W4A16_ERR_CAPACITY);
+    cta_cnt[e] = c;
+  }
+  cluster.sync();   // every CTA's totals are final
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int b = 0, t = 0;
+    for (int r = 0; r < kAlignCtas; ++r) {
+      const int c = *cluster.map_shared_rank(cta_cnt + e, r);
+      if (r < rank) b += c;
+      t += c;
+    }
+    before[e] = b;
+    tot[e] = t;
+    if (rank == 0) {
+      if (counts != nullptr) counts[e] = t;
+      if (masked && t > max_m) set_error(err, MOE_W4A16_ERR_CAPACITY);
+    }
   }
   __syncthreads();
   if (warp == 0) {
     int carry = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
+    for (int b0 = 0; b0 < E; b0 += 32) {
+      const int e = b0 + lane;
       int padded = 0;
-      if (e < E) padded = masked ? max_m : ((cnt[e] + block_m - 1) / block_m) * block_m;
+      if (e < E) padded = masked ? max_m : ((tot[e] + block_m - 1) / block_m) * block_m;
       int v = padded;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -68,14 +92,14 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(const int32_t* 
     if (lane == 0) start[E] = carry;
   }
   __syncthreads();
-  for (int base = beg; base < end; base += 32) {
-    const int i = base + lane;
+  for (int b0 = beg; b0 < end; b0 += 32) {
+    const int i = b0 + lane;
     const int e = i < end ? ids[i] : -1;
     const bool valid = e >= 0 && e < E;
     const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int rk = __popc(peers & ((1u << lane) - 1u));
     int off = 0;
-    if (valid) off = hist[warp * E + e] + rank;
+    if (valid) off = before[e] + hist[warp * E + e] + rk;
     __syncwarp();
     if (valid) {
       if (lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
@@ -87,20 +111,20 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(const int32_t* 
     }
     __syncwarp();
   }
-  __syncthreads();
-  // padding: sentinels / -1 fill and the expert of every block
-  for (int e = warp; e < E; e += kAlignWarps) {
-    const int c = masked ? min(cnt[e], max_m) : cnt[e];
-    const int s = start[e], s_end = start[e + 1];
-    for (int pos = s + c + lane; pos < s_end; pos += 32) {
+  // padding: sentinels / -1 fill and the expert of every block (experts split over the cluster)
+  for (int e = rank + kAlignCtas * warp; e < E; e += kAlignCtas * kAlignWarps) {
+    const int c = masked ? min(tot[e], max_m) : tot[e];
+    const int s0 = start[e], s_end = start[e + 1];
+    for (int pos = s0 + c + lane; pos < s_end; pos += 32) {
       if (masked) masked_rows[pos] = -1;
       else sorted_ids[pos] = R;
     }
     if (!masked) {
-      for (int b = s / block_m + lane; b < s_end / block_m; b += 32) expert_ids[b] = e;
+      for (int b = s0 / block_m + lane; b < s_end / block_m; b += 32) expert_ids[b] = e;
     }
   }
-  if (!masked && threadIdx.x == 0) *npp = start[E];
+  if (!masked && rank == 0 && threadIdx.x == 0) *npp = start[E];
+  cluster.sync();   // no CTA leaves while another may still read its shared memory
 }
 
 __global__ void contiguous_layout_kernel(const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ expert_ids,
@@ -284,17 +308,17 @@ cudaError_t launch_gather_sorted(const uint16_t* src, int64_t src_rows, int K, c
 cudaError_t launch_align(const int32_t* topk_ids, int R, int E, int block_m, int max_m, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* num_post_padded, int32_t* counts, int32_t* masked_rows,
                          int* err, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(kAlignWarps * E + 2 * E + 1) * sizeof(int);
+  const size_t smem = static_cast<size_t>(kAlignWarps * E + 4 * E + 1) * sizeof(int);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>((kAlignWarps * MOE_W4A16_MAX_EXPERTS + 2 * MOE_W4A16_MAX_EXPERTS + 1) * sizeof(int)));
+                                         static_cast<int>((kAlignWarps * MOE_W4A16_MAX_EXPERTS + 4 * MOE_W4A16_MAX_EXPERTS + 1) * sizeof(int)));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  align_kernel<<<1, kAlignWarps * 32, smem, stream>>>(topk_ids, R, E, block_m, max_m, sorted_ids, expert_ids,
+  align_kernel<<<kAlignCtas, kAlignWarps * 32, smem, stream>>>(topk_ids, R, E, block_m, max_m, sorted_ids, expert_ids,
                                                       num_post_padded, counts, masked_rows, err);
   note_launch();
   return cudaGetLastError();
