@@ -13,8 +13,8 @@
 //                 A operand in TMEM, B in shared memory; one thread issues an
 //                 MMA only every ~100 cycles, so the tiles get a thread each
 //   warp 2      : loads the block's activation rows per k-chunk with TMA into
-//                 a 128-byte-swizzled K-major tile (16-row boxes when the rows
-//                 are consecutive, tile::gather4 otherwise)
+//                 a 128-byte-swizzled K-major tile (16-row boxes: a block's rows
+//                 are consecutive -- indexed calls gather them in slot order first)
 //   warps 4-19  : dequantise one 16-channel m-tile each per k-chunk in
 //                 registers and store it to TMEM as the MMA's A operand
 //                 (tcgen05.st), then run the epilogue from TMEM
@@ -66,8 +66,7 @@ constexpr int kPOff = kXOff + kXStages * kXBytes;
 constexpr int kBarOff = kPOff + kPStages * kPBytes;
 constexpr int kNumBars = 2 * kPStages + 2 * kXStages + 2 * kWStages + 3;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kXRowOff = kMiscOff + 16;             // int [kRows] activation row table
-constexpr int kPrefixOff = kXRowOff + kRows * 4;
+constexpr int kPrefixOff = kMiscOff + 16;           // masked: int [E + 1] block prefix
 // TMEM (512 columns x 128 lanes x 32 bit): FP32 accumulators of the two 128-channel tiles at
 // columns [0, kRows) and [kRows, 2 kRows); dequantised BF16 weights, the MMA's A operand
 // (lane = channel, column c = k pair 2c, 2c+1), in kWStages stages of 2 tiles x 32 columns.
@@ -149,16 +148,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tma
       : "memory");
 }
 
-// 4 rows of a 2-D tensor (box: 64 bf16 x 1 row, 128-byte swizzle) -> 512 B of shared memory.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tmap, int x, int y0, int y1, int y2,
-                                            int y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
-}
-
 // K-major operand with 128-byte swizzle: rows of 128 B, 8-row atoms of 1024 B.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
@@ -204,8 +193,7 @@ __device__ __forceinline__ int block_extent(const GemmParams& p, int blk, int e,
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
-                        const __grid_constant__ CUtensorMap tmap_tile) {
+    prefill_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_tile) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -217,7 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t acc_full = w_empty + 8 * kWStages, acc_empty = acc_full + 8, drain_bar = acc_empty + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
-  int* xrow_tab = reinterpret_cast<int*>(smem + kXRowOff);
   int* prefix = reinterpret_cast<int*>(smem + kPrefixOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -254,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nblk = num_row_blocks(p, rows_per_block, prefix);
   const int64_t total_units = static_cast<int64_t>(nblk) * p.NG;
   PipeStats ps;
-  int stats_base = -1;
+  [[maybe_unused]] int stats_base = -1;
 
   if (warp == 0) {
     // ----------------------------------------------------- packed weights
@@ -369,10 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ----------------------------------------------------- activation rows
-    // TMA gather: one tile::gather4 copies 4 rows x 128 B into the swizzled tile;
-    // padding rows up to the 16-row MMA edge repeat row 0 (their columns are not stored).
+    // 16-row 2-D boxes of the block's consecutive rows; rows past the block up to the
+    // 16-row MMA edge are whatever follows (or the fill value), their columns are not stored.
     stats_base = 16;
-    int* xrow = xrow_tab;
     int stage = 0;
     uint32_t phase = 0;
     bool issued = false;
@@ -385,17 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ext = block_extent(p, blk, e, local, rows_per_block);
       if (ext == 0) continue;
       const int nr = (ext + 15) & ~15;
-      // contiguous / masked blocks hold consecutive rows: whole 16-row boxes
-      const bool consecutive = p.layout != MOE_W4A16_LAYOUT_INDEXED || p.a_sorted;
-      const int row0 = consecutive ? block_row(p, blk, e, local, rows_per_block, 0).a_row : 0;
-      __syncwarp();
-      if (!consecutive) {
-        for (int i = lane; i < nr; i += 32) {
-          const int ar = (i < ext) ? block_row(p, blk, e, local, rows_per_block, i).a_row : -1;
-          xrow[i] = ar < 0 ? 0 : ar;
-        }
-      }
-      __syncwarp();
+      const int row0 = block_row(p, blk, e, local, rows_per_block, 0).a_row;
       for (int kc = 0; kc < p.KC; ++kc) {
         ps.start();
         if (!warp_wait(x_empty + 8 * stage, phase ^ 1u, abort_flag, p.err)) goto x_done;
@@ -404,15 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nr) * 128u);
         __syncwarp();
         const uint32_t xa = sbase + kXOff + stage * kXBytes;
-        if (consecutive) {
-          for (int g16 = lane; g16 < (nr >> 4); g16 += 32)
-            tma_load_2d(xa + g16 * 2048, &tmap_tile, kc * kChunkK, row0 + 16 * g16, full);
-        } else {
-          for (int g4 = lane; g4 < (nr >> 2); g4 += 32) {
-            const int* r4 = xrow + 4 * g4;
-            tma_gather4(xa + g4 * 512, &tmap_a, kc * kChunkK, r4[0], r4[1], r4[2], r4[3], full);
-          }
-        }
+        for (int g16 = lane; g16 < (nr >> 4); g16 += 32)
+          tma_load_2d(xa + g16 * 2048, &tmap_tile, kc * kChunkK, row0 + 16 * g16, full);
         issued = true;
         if (++stage == kXStages) {
           stage = 0;
@@ -590,19 +559,14 @@ EncodeTiledFn encode_tiled() {
 
 cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
   using namespace prefill;
-  // activations as a 2-D tensor [a_rows, K] of bf16, read 4 rows x 128 B at a time by tile::gather4
+  // a block's rows must be consecutive in A (indexed calls gather them in slot order first)
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED && !p.a_sorted) return cudaErrorInvalidValue;
+  // activations as a 2-D tensor [a_rows, K] of bf16, read in 16-row x 128-byte boxes
   EncodeTiledFn enc = encode_tiled();
   if (enc == nullptr || p.a_rows < 1) return cudaErrorNotSupported;
-  CUtensorMap tmap;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.a_rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkK), 1};
   const cuuint32_t estr[2] = {1, 1};
-  if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.a), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  // the same tensor with 16-row boxes for blocks of consecutive rows
   CUtensorMap tmap_tile;
   const cuuint32_t box16[2] = {static_cast<cuuint32_t>(kChunkK), 16};
   if (enc(&tmap_tile, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.a), dims, strides, box16, estr,
@@ -627,7 +591,7 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
   int64_t grid = di.sm_count;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  prefill_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p, tmap, tmap_tile);
+  prefill_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p, tmap_tile);
   note_launch();
   if (grid_out) *grid_out = static_cast<int>(grid);
   return cudaGetLastError();
