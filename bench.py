@@ -50,6 +50,7 @@ WORKLOAD_ALIASES = {
     "decode_gate_up_masked": ("decode_gate_up", "masked"),
     "decode_down_combine": ("decode_down_combine", "indexed"),
     "tiny_indexed": ("tiny_indexed", "indexed"),
+    "tp8_decode_gate_up_masked": ("tp8_decode_gate_up", "masked"),
 }
 
 

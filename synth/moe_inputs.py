@@ -130,6 +130,19 @@ WORKLOADS: Dict[str, Workload] = {
             description="prefill MoE FFN: 8192 tokens, 384 experts, top-8 (about 171 rows/expert), gate_up "
                         "7168->4096, SiLU(gate)*up, down 2048->7168, weighted top-8 combine",
         ),
+        # tensor-parallel shards of the same layer (8 ranks: intermediate 2048 / 8 per rank)
+        Workload(
+            name="tp8_decode_gate_up", num_tokens=64, num_experts=384, top_k=8, hidden=7168, intermediate=256,
+            stage="gate_up", routing="skewed", max_m=16,
+            description="one rank of an 8-way tensor-parallel decode gate_up: 64 tokens, 384 experts, top-8 "
+                        "skewed routing, K=7168, N=512",
+        ),
+        Workload(
+            name="tp8_prefill_ffn", num_tokens=8192, num_experts=384, top_k=8, hidden=7168, intermediate=256,
+            stage="ffn", routing="softmax",
+            description="one rank of an 8-way tensor-parallel prefill FFN: 8192 tokens, 384 experts, top-8, "
+                        "gate_up 7168->512, SiLU(gate)*up, down 256->7168 (partial sums of the layer's output)",
+        ),
     ]
 }
 

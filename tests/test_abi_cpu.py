@@ -77,6 +77,17 @@ def test_workspace_size(lib):
     # masked / decode-family indexed calls: header only
     assert f(2, 128, 8, 384, 7168, 2048, 0, 0, ctypes.byref(out)) == 0 and out.value == 256
     assert f(0, 128, 8, 384, 7168, 2048, 32, 0, ctypes.byref(out)) == 0 and out.value == 256
+    # narrow outputs (n <= 1024) on the decode kernel: + the partial tiles of units cut into 4 k-ranges when
+    # a call has at most 120 units (120 units x 4 parts x 8 warps x 32 lanes x FP32 values: 16 for 16-row
+    # blocks, 32 for 32-row blocks and masked calls) + their counters
+    cut16 = 120 * 4 * 8 * 16 * 32 * 4 + 120 * 8 * 4
+    cut32 = 120 * 4 * 8 * 32 * 32 * 4 + 120 * 8 * 4
+    assert f(0, 64, 8, 384, 512, 7168, 16, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut16
+    assert f(0, 64, 8, 384, 1024, 7168, 32, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut32
+    assert f(2, 64, 8, 384, 512, 7168, 0, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut32
+    assert f(0, 64, 8, 384, 1280, 7168, 16, 0, ctypes.byref(out)) == 0 and out.value == 256
+    cap = 64 * 8 + 384 * 63                         # tcgen05 block sizes: gathered rows, no partial tiles
+    assert f(0, 64, 8, 384, 512, 7168, 64, 0, ctypes.byref(out)) == 0 and out.value == 256 + cap * 7168 * 2
     # combine: arrival counters + routed-row staging
     assert f(0, 128, 8, 384, 7168, 2048, 32, 2 | 4, ctypes.byref(out)) == 0
     counters = -(-(128 * 28 * 8 * 4) // 256) * 256
@@ -113,7 +124,7 @@ def _desc(mode=1, e=4, n=256, k=128):
 FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails its host-side checks
 
 
-def _masked(lib, d, flags=0, ws_bytes=256, k=128, expected_m=1):
+def _masked(lib, d, flags=0, ws_bytes=1 << 30, k=128, expected_m=1):
     return lib.moe_w4a16_masked(FAKE, ctypes.c_int(d.num_experts), 16, k, FAKE, expected_m, ctypes.byref(d), FAKE,
                                 None, 8, 2, None, ctypes.c_uint32(flags), FAKE, FAKE, ctypes.c_size_t(ws_bytes),
                                 None)
@@ -143,14 +154,14 @@ def test_gemm_host_checks_reject_before_launch(lib):
 
 
 def test_noalloc_rejects_before_any_cuda_call(lib):
-    """The static-scratch entry point refuses calls whose scratch exceeds 16 MiB, and prefill block sizes."""
+    """The static-scratch entry point refuses calls whose scratch exceeds 32 MiB, and prefill block sizes."""
     d = _desc(e=4, n=1024, k=64)
 
     def call(t, k, block_m, flags, desc=d):
         return lib.moe_w4a16_indexed_noalloc(FAKE, t * k, 64, ctypes.byref(desc) if desc else None, FAKE, FAKE, FAKE, FAKE, t, k, block_m, FAKE,
                                              ctypes.c_uint32(flags), FAKE, None, None)
 
-    assert call(1100, 8, 16, 2 | 4) == 9              # 256 + counters + 1100*8*1024*2 B > 16 MiB
+    assert call(2000, 8, 16, 2 | 4) == 9              # counters + 2000*8*1024*2 B + partial tiles > 32 MiB
     assert call(8, 8, 64, 0) == 1                     # block_m above 32 runs the prefill kernel: refused
     assert call(8, 8, 0, 0) == 1
     assert call(8, 8, 16, 0, desc=None) == 1

@@ -5,11 +5,13 @@ same plan, same sequence of library calls), runs one step, and compares
 outputs with the oracle:
 
 * the 64-token, 8-expert indexed GEMM: every output element;
-* decode gate_up, 384 experts, top-8 skewed (indexed and masked layouts):
-  every routed row of four experts (hottest, median, coldest active, and
-  the expert of token 0) on a sample of output channels;
+* decode gate_up, 384 experts, top-8 skewed (indexed and masked layouts),
+  at N=4096 and at one 8-way tensor-parallel shard's N=512: every routed
+  row of four experts (hottest, median, coldest active, and the expert of
+  token 0) on a sample of output channels;
 * decode down + top-8 combine, 128 tokens: 16 tokens on a channel sample;
-* prefill FFN, 8192 tokens (indexed and contiguous layouts): the SwiGLU rows
+* prefill FFN, 8192 tokens (indexed and contiguous layouts; and the indexed
+  layout at the tensor-parallel shard's intermediate 256): the SwiGLU rows
   of every routed row of token 0's eight experts, all intermediate channels,
   then token 0's combined output on a channel sample;
 * the gate_up schedule sweep, 16..16384 tokens, uniform and Zipf skew:
@@ -111,7 +113,8 @@ def _sample_experts(counts, ids):
     return list(dict.fromkeys(int(e) for e in picks))
 
 
-@pytest.mark.parametrize("name", ["decode_gate_up", "decode_gate_up_masked"])
+@pytest.mark.parametrize("name", ["decode_gate_up", "decode_gate_up_masked", "tp8_decode_gate_up",
+                                  "tp8_decode_gate_up_masked"])
 def test_decode_gate_up_sampled(name):
     arm, wl = _arm(name)
     out = arm.step()
@@ -151,10 +154,10 @@ def test_decode_down_combine_sampled():
     assert_close(_gpu_rows(out, tokens, chans), ref, "decode down+combine", slack=slack)
 
 
-@functools.lru_cache(maxsize=1)
-def _prefill_token0_reference():
+@functools.lru_cache(maxsize=2)
+def _prefill_token0_reference(base):
     """Oracle SwiGLU rows of every routed row of token 0's experts, and token 0's combined output."""
-    wl = S.get_workload("prefill_ffn")
+    wl = S.get_workload(base)
     ids, wts = S.routing(wl)
     a = S.activations(wl.seed, wl.num_tokens, wl.hidden)
     k = wl.top_k
@@ -173,7 +176,7 @@ def _prefill_token0_reference():
     return h_rows, chans, O.combine(y2, wts[:1]), combine_slack(y2, wts[:1])
 
 
-@pytest.mark.parametrize("name", ["prefill_ffn", "prefill_ffn_contiguous"])
+@pytest.mark.parametrize("name", ["prefill_ffn", "prefill_ffn_contiguous", "tp8_prefill_ffn"])
 def test_prefill_ffn_sampled(name):
     arm, wl = _arm(name)
     f = arm.ffn
@@ -187,7 +190,7 @@ def test_prefill_ffn_sampled(name):
     where = np.full(wl.rows, -1, dtype=np.int64)
     valid = (slot_ids >= 0) & (slot_ids < wl.rows)
     where[slot_ids[valid]] = np.nonzero(valid)[0]
-    h_rows, chans, ref0, slack0 = _prefill_token0_reference()
+    h_rows, chans, ref0, slack0 = _prefill_token0_reference(wl.name)
     for e, (flat, href) in h_rows.items():
         assert (where[flat] >= 0).all()
         assert_close(_gpu_rows(h, where[flat]), href, f"{name} SwiGLU rows of expert {e}")

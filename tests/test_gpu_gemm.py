@@ -12,8 +12,8 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_util import (assert_close, bits_to_dev, dev_to_bits, distinct_topk, i32_to_dev, ids_from_counts,
-                      prepare_dev, random_acts, random_weights)
+from gpu_util import (assert_close, bits_to_dev, combine_slack, dev_to_bits, distinct_topk, i32_to_dev,
+                      ids_from_counts, prepare_dev, random_acts, random_weights)
 
 pytestmark = pytest.mark.gpu
 
@@ -330,3 +330,30 @@ def test_plan_picks_family_and_block_from_rows_per_expert(tokens, kernel, block_
     assert s.tok_e == -(-tokens * 8 // 384)
     m = M.plan(M.LAYOUT_MASKED, tokens, 8, 384, 4096, 7168, expected_m=s.tok_e)
     assert m.kernel == kernel
+
+
+@pytest.mark.parametrize("e,t,k,kd,flags", [(30, 100, 4, 448, 0), (100, 400, 4, 448, 0), (24, 60, 4, 192, "combine"),
+                                            (3, 5, 2, 64, 0)])
+def test_narrow_output_cut_units(e, t, k, kd, flags):
+    """N=512 (two 256-channel groups): at most 120 (row block, group) units cut every unit into k-ranges summed
+    in part order (K chunks 7: parts of 1/2 chunks; 3 chunks: three parts; 1 chunk: one part), more units do not
+    cut; both match the oracle and repeat bit-identically."""
+    n, bm = 512, 16
+    rng = np.random.default_rng(700 + e + t)
+    ids = distinct_topk(rng, t, e, k)
+    counts = np.bincount(ids.reshape(-1), minlength=e)
+    units = int(np.sum(-(-counts // bm))) * (n // 256)
+    assert (units <= 120) == (t < 400)
+    comb = flags == "combine"
+    a = random_acts(rng, t * k if comb else t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    w = rng.uniform(0, 1, size=(t, k)).astype(np.float32) if comb else None
+    y = O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), n, a_per_routed_row=comb)
+    f = M.FLAG_COMBINE if comb else 0
+    runs = [_indexed_run(a, qw, sc, ids, bm, flags=f, weights=w, a_per_row=comb) for _ in range(3)]
+    if comb:
+        assert_close(runs[0], O.combine(y, w), f"cut units e={e} t={t} combine", slack=combine_slack(y, w))
+    else:
+        assert_close(runs[0], y, f"cut units e={e} t={t}")
+    for r in runs[1:]:
+        assert np.array_equal(r, runs[0])

@@ -189,8 +189,19 @@ struct WsLayout {
   size_t y_off = 0, y_bytes = 0;
   size_t cb_off = 0;
   int cb_segs = 0;   // contiguous: segments the merged block table holds
+  size_t cut_off = 0, cut_bytes = 0, cutc_off = 0;
   size_t total = 0;
 };
+
+// Rows per block for which the decode kernel's cut-unit partial tiles are sized (0: the call does
+// not run the decode kernel with cut units: prefill block sizes, or an output wider than
+// kCutMaxGroups groups). Masked row budgets are not known here: 32-row size.
+static int cut_rows(int layout, int block_m, int n) {
+  if (n > kCutMaxGroups * kGroupN) return 0;
+  if (layout == MOE_W4A16_LAYOUT_MASKED) return kDecodeRows;
+  if (layout != MOE_W4A16_LAYOUT_INDEXED || block_m < 1 || block_m > kDecodeRows) return 0;
+  return block_m <= kDecodeRowsSmall ? kDecodeRowsSmall : kDecodeRows;
+}
 
 static bool gathers_activations(int layout, int block_m, uint32_t flags) {
   return layout == MOE_W4A16_LAYOUT_INDEXED && block_m > kDecodeRows && !(flags & MOE_W4A16_FLAG_A_SORTED);
@@ -228,6 +239,13 @@ static moe_w4a16_status ws_layout(int layout, int num_tokens, int top_k, int num
     L->cb_segs = static_cast<int>(segs < static_cast<size_t>(kMaxContigSegs) ? segs : kMaxContigSegs);
     L->cb_off = off;
     off += align_up((static_cast<size_t>(L->cb_segs) + 1) * 16, 256);
+  }
+  if (const int rows = cut_rows(layout, block_m, n)) {
+    L->cut_off = off;
+    L->cut_bytes = cut_partial_bytes(rows);
+    off += L->cut_bytes;
+    L->cutc_off = off;
+    off += align_up(kCutCounterBytes, 256);
   }
   L->total = off;
   return MOE_W4A16_OK;
@@ -460,6 +478,11 @@ static void fill_common(GemmParams& p, const moe_w4a16_desc* desc, const void* p
   if (flags & MOE_W4A16_FLAG_COMBINE) {
     p.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + L.counters_off);
     p.y_ws = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.y_off);
+  }
+  if (L.cut_bytes) {
+    p.sk_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.cut_off);
+    p.sk_counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + L.cutc_off);
+    p.sk_units = kMaxCutUnits;
   }
 }
 

@@ -87,9 +87,9 @@ __device__ __forceinline__ void store_bf16(uint16_t* base, int64_t idx, float v)
 // stage, a lane loads its four FU words of each chunk, its scales, and the
 // activation B fragments of NT tiles, releases the stage, then dequantises
 // 8 FUs and issues 8*NT MMAs. Returns false when a wait gave up.
-template <int ROWS, int NT>
+template <int ROWS, int NT, bool CUT>
 __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s, int& stage, uint32_t& phase,
-                                             uint32_t wq_off, uint32_t sc_off, int lane,
+                                             uint32_t wq_off, uint32_t sc_off, int lane, int nkc,
                                              float (&acc)[2][Geo<ROWS>::kTiles][4], PipeStats& ps) {
 #pragma unroll
   for (int c = 0; c < 2; ++c)
@@ -98,7 +98,8 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
   const uint32_t act_lane = 2 * kChunkBytes + (lane & 7) * kActStride + (lane >> 3) * 16;
-  for (int kc = 0; kc < p.KC; ++kc) {
+  const int kcs = CUT ? nkc : p.KC;   // the uncut variant reads K-chunks from the parameters
+  for (int kc = 0; kc < kcs; ++kc) {
     ps.start();
     if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) return false;
     ps.stop(0);
@@ -146,7 +147,77 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
   return true;
 }
 
+// Pieces handed out by the unit counter: whole units in order, except that a call
+// with a narrow output (at most kCutMaxGroups 256-channel groups, e.g. one
+// tensor-parallel shard) and at most kMaxCutUnits units has every unit cut into
+// kParts k-ranges so that more CTAs stream weights. The Chord page (section "H200
+// prefill and TP8") gives TP8 its own flatter tiling for the same reason: a narrow
+// intermediate leaves few N tiles per SM. A cut unit is summed by the last of its
+// parts to arrive, parts in order. The choice depends on N and the unit count
+// alone, not on the grid, so a call's result does not depend on how it was launched.
+struct Piece {
+  int u, kc0, kc1, part;  // part -1: a whole unit
+};
+
+__device__ __forceinline__ int split_units(int64_t U, const GemmParams& p) {
+  if (p.sk_partials == nullptr || U > p.sk_units) return 0;
+  return static_cast<int>(U);
+}
+
+// Piece `idx` of a call with U units of KC k-chunks and X cut units (false: none left).
+__device__ __forceinline__ bool piece_of(int64_t idx, int64_t U, int X, int KC, Piece& pc) {
+  const int parts = KC < kParts ? KC : kParts;
+  const int64_t whole = U - X;
+  if (idx < whole) {
+    pc.u = static_cast<int>(idx);
+    pc.kc0 = 0;
+    pc.kc1 = KC;
+    pc.part = -1;
+    return true;
+  }
+  const int64_t q = idx - whole;
+  if (q >= static_cast<int64_t>(X) * parts) return false;
+  const int su = static_cast<int>(q / parts), part = static_cast<int>(q % parts);
+  pc.u = static_cast<int>(whole) + su;
+  pc.kc0 = KC * part / parts;
+  pc.kc1 = KC * (part + 1) / parts;
+  pc.part = part;
+  return true;
+}
+
+// Part `part` of cut unit `su`: store this warp's FP32 partial tile; the warp that
+// brings the last part adds the parts in part order (deterministic) and returns true
+// to run the epilogue. Layout [su][part][warp][value][lane]. Not inlined: it runs
+// once per cut unit and keeps its registers out of the K loop.
 template <int ROWS>
+__device__ __noinline__ bool part_fixup(const GemmParams& p, int su, int part, int parts, int warp, int lane,
+                                        float* acc) {
+  constexpr int V = 2 * Geo<ROWS>::kTiles * 4;
+  auto slot = [&](int q) {
+    return p.sk_partials + ((static_cast<size_t>(su) * kParts + q) * kConsumerWarps + warp) * V * 32;
+  };
+  float* mine = slot(part);
+  for (int v = 0; v < V; ++v) mine[v * 32 + lane] = acc[v];
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(p.sk_counters + su * kConsumerWarps + warp, 1) == parts - 1;
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return false;
+  __threadfence();
+  if (lane == 0) p.sk_counters[su * kConsumerWarps + warp] = 0;   // zero again for the next call
+  for (int v = 0; v < V; ++v) {
+    float sum = 0.f;
+    for (int q = 0; q < parts; ++q) {
+      const float y = q == part ? acc[v] : __ldcg(slot(q) + v * 32 + lane);
+      sum = q == 0 ? y : sum + y;
+    }
+    acc[v] = sum;
+  }
+  return true;
+}
+
+template <int ROWS, bool CUT>
 __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_kernel(const GemmParams p) {
   using G = Geo<ROWS>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -182,13 +253,18 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     uint32_t phase = 0;
     bool issued_any = false;
     PipeStats pps;
+    const int X = CUT ? split_units(total_units, p) : 0;
     while (true) {
-      // units are handed out in order, one at a time, to whichever CTA asks next
-      int64_t u = 0;
-      if (lane == 0) u = atomicAdd(p.grab, 1);
-      u = __shfl_sync(0xffffffffu, u, 0);
-      if (u >= total_units) break;
-      const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
+      // pieces are handed out in order, one at a time, to whichever CTA asks next
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(p.grab, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      Piece pc{idx, 0, p.KC, -1};
+      if (CUT ? !piece_of(idx, total_units, X, p.KC, pc) : idx >= total_units) break;
+      const int u = pc.u;
+      // (the uncut variant divides in 64 bits: with it ptxas allocates that kernel without spills)
+      const int blk = CUT ? u / p.NG : static_cast<int>(static_cast<int64_t>(u) / p.NG);
+      const int gp = CUT ? u % p.NG : static_cast<int>(static_cast<int64_t>(u) % p.NG);
       int local;
       const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
       if (e < 0) continue;
@@ -206,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
         asrc[j] = ar >= 0 ? p.a + static_cast<int64_t>(ar) * p.K + (lane & 7) * 8 : nullptr;
       }
       const uint32_t adst = 2 * kChunkBytes + (lane >> 3) * kActStride + (lane & 7) * 16;
-      for (int kc = 0; kc < p.KC; ++kc) {
+      const int kc0 = CUT ? pc.kc0 : 0, kc1 = CUT ? pc.kc1 : p.KC;
+      for (int kc = kc0; kc < kc1; ++kc) {
         pps.start();
         if (!warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err)) goto producer_done;
         pps.stop(0);
@@ -214,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
         const uint32_t full = s.full + 8 * stage;
         const uint32_t sb = s.stages + stage * G::kStageBytes;
         if (lane == 0) {
-          if (kc == 0) desc[stage] = static_cast<int>(u);
+          if (kc == kc0) desc[stage] = idx;
           mbar_arrive_expect_tx(full, kPairBytes);
           bulk_g2s_hint(sb, wsrc + static_cast<size_t>(kc) * kPairBytes, kPairBytes, full, pol);
         }
@@ -261,13 +338,16 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     const uint32_t wq_off = (warp * 32 + lane) * 16;
     const uint32_t sc_off = kChunkWBytes + (warp * 8 + g) * 8;
     PipeStats cps;
+    const int X = CUT ? split_units(total_units, p) : 0;
     while (true) {
       cps.stop(3);   // epilogue of the previous unit (and unit bookkeeping)
-      // the next unit is the one the producer put at the head of the current stage
+      // the next piece is the one the producer put at the head of the current stage
       if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) goto consumer_done;
-      const int u = desc[stage];
-      if (u < 0) break;
-      const int blk = static_cast<int>(u / p.NG), gp = static_cast<int>(u % p.NG);
+      const int idx = desc[stage];
+      Piece pc{idx, 0, p.KC, -1};
+      if (idx < 0 || (CUT && !piece_of(idx, total_units, X, p.KC, pc))) break;
+      const int u = pc.u;
+      const int blk = u / p.NG, gp = u % p.NG;
       int local;
       const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
       if (e < 0) break;   // never: the producer hands out only units with work
@@ -277,20 +357,34 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       const int ntiles = (32 - __clz(vmask) + 7) >> 3;
 
       float acc[2][G::kTiles][4];
+      const int nkc = pc.kc1 - pc.kc0;
       bool ok;
       cps.start();
       const long long t_unit = clock64();
       switch (ntiles) {
-        case 1: ok = consume_unit<ROWS, 1>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
-        case 2: ok = consume_unit<ROWS, 2>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
-        case 3: ok = consume_unit<ROWS, (G::kTiles > 2 ? 3 : 2)>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps);
-                break;
-        default: ok = consume_unit<ROWS, G::kTiles>(p, s, stage, phase, wq_off, sc_off, lane, acc, cps); break;
+        case 1: ok = consume_unit<ROWS, 1, CUT>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
+        case 2: ok = consume_unit<ROWS, 2, CUT>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
+        case 3:
+          ok = consume_unit<ROWS, (G::kTiles > 2 ? 3 : 2), CUT>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps);
+          break;
+        default: ok = consume_unit<ROWS, G::kTiles, CUT>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
       }
       cps.add(2, static_cast<unsigned long long>(clock64() - t_unit));
       cps.add(4, 1);
       cps.start();
       if (!ok) goto consumer_done;
+      if (CUT && pc.part >= 0) {
+        // a cut unit: only the last of its parts runs the epilogue
+        constexpr int V = 2 * G::kTiles * 4;
+        float part[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) part[v] = acc[v / (4 * G::kTiles)][(v / 4) % G::kTiles][v % 4];
+        if (!part_fixup<ROWS>(p, u - static_cast<int>(total_units - X), pc.part, p.KC < kParts ? p.KC : kParts, warp,
+                              lane, part))
+          continue;
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v / (4 * G::kTiles)][(v / 4) % G::kTiles][v % 4] = part[v];
+      }
 
       // ---------------------------------------------------------- epilogue
       // acc[c][nt]: channels ch = c*128 + warp*16 + g (+8), token slots nt*8 + 2t (+1)
@@ -380,14 +474,14 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
 
 namespace decode {
 
-template <int ROWS>
+template <int ROWS, bool CUT>
 cudaError_t launch_rows(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
   using G = Geo<ROWS>;
   const DeviceInfo& di = device_info(device);
   const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
   static bool attr_set[64] = {false};
   if (device >= 0 && device < 64 && !attr_set[device]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<ROWS, CUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          G::smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
     if (e != cudaSuccess) return e;
     attr_set[device] = true;
@@ -401,7 +495,7 @@ cudaError_t launch_rows(const GemmParams& p, int device, cudaStream_t stream, in
   int64_t grid = static_cast<int64_t>(di.sm_count) * G::kCtasPerSm;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  decode_gemm_kernel<ROWS><<<static_cast<int>(grid), kThreads, G::smem_bytes(prefix_entries), stream>>>(p);
+  decode_gemm_kernel<ROWS, CUT><<<static_cast<int>(grid), kThreads, G::smem_bytes(prefix_entries), stream>>>(p);
   note_launch();
   if (grid_out) *grid_out = static_cast<int>(grid);
   return cudaGetLastError();
@@ -410,12 +504,19 @@ cudaError_t launch_rows(const GemmParams& p, int device, cudaStream_t stream, in
 }  // namespace decode
 
 // Row blocks of at most 16 rows (indexed block_m <= 16, masked budget <= 16) run
-// the 16-row variant; contiguous blocks and larger ones the 32-row variant.
+// the 16-row variant; contiguous blocks and larger ones the 32-row variant. Narrow
+// outputs (at most kCutMaxGroups 256-channel groups, e.g. a tensor-parallel shard's
+// gate_up) run the variant that may cut units into k-ranges; the others keep a K
+// loop without that bookkeeping (its registers cost 3-4% on the wide shapes).
 cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
   const bool small = (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.block_m <= kDecodeRowsSmall) ||
                      (p.layout == MOE_W4A16_LAYOUT_MASKED && p.max_m <= kDecodeRowsSmall);
-  return small ? decode::launch_rows<kDecodeRowsSmall>(p, device, stream, grid_out)
-               : decode::launch_rows<kDecodeRows>(p, device, stream, grid_out);
+  const bool cut = p.sk_partials != nullptr && p.NG <= kCutMaxGroups;
+  if (small)
+    return cut ? decode::launch_rows<kDecodeRowsSmall, true>(p, device, stream, grid_out)
+               : decode::launch_rows<kDecodeRowsSmall, false>(p, device, stream, grid_out);
+  return cut ? decode::launch_rows<kDecodeRows, true>(p, device, stream, grid_out)
+             : decode::launch_rows<kDecodeRows, false>(p, device, stream, grid_out);
 }
 
 }  // namespace moe

@@ -82,7 +82,10 @@ struct GemmParams {
   int num_tokens, top_k;
   uint16_t* y_ws;            // bf16 [R, N] staging
   int* counters;             // [num_tokens, NG]
-  int* grab;                 // decode: [0] next unit to hand out, [1] CTAs done (zero between calls)
+  int* grab;                 // decode: [0] next piece to hand out, [1] CTAs done (zero between calls)
+  float* sk_partials;        // decode: FP32 partial tiles of cut units [sk_units][kParts][8][values][32]
+  int* sk_counters;          // decode: arrival counters of cut units [sk_units][8] (zero between calls)
+  int sk_units;              // cut units the partial region holds
 
   // output
   uint16_t* c;
@@ -119,6 +122,17 @@ cudaError_t launch_combine_rows(const uint16_t* y, const float* w, int T, int to
 // Returns the number of CTAs launched through *grid_out.
 cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out);
 cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out);
+
+// Decode: a call with at most kCutMaxGroups 256-channel groups and at most kMaxCutUnits
+// units has every unit cut into kParts k-ranges.
+constexpr int kParts = 4;
+constexpr int kMaxCutUnits = 120;
+constexpr int kCutMaxGroups = 4;
+// Bytes of the cut-unit partial tiles for blocks of `rows` rows (16 or 32) and of their counters.
+constexpr size_t cut_partial_bytes(int rows) {
+  return static_cast<size_t>(kMaxCutUnits) * kParts * 8 * (2 * (rows / 8) * 4) * 32 * sizeof(float);
+}
+constexpr size_t kCutCounterBytes = static_cast<size_t>(kMaxCutUnits) * 8 * sizeof(int);
 
 // Rows per block the kernels use for the contiguous / masked layouts.
 constexpr int kDecodeRows = 32;

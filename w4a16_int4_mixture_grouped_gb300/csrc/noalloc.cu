@@ -6,8 +6,9 @@
 // that owns no torch (or other) caching allocator to hand out a workspace.
 // The call runs the same decode kernel as moe_w4a16_indexed (block_m <= 32)
 // and takes its scratch -- the device error word, the combine arrival
-// counters and the combine staging rows -- from kStaticScratchBytes of
-// statically reserved device memory instead of a caller workspace.
+// counters, the combine staging rows and the decode kernel's partial tiles
+// and counters -- from kStaticScratchBytes of statically reserved device
+// memory instead of a caller workspace.
 //
 // Set-up: the first call on a device, with that device current, resolves the
 // array's address once (cudaGetSymbolAddress, which also loads this module on
@@ -16,8 +17,10 @@
 //
 // Sharing: every call on a device uses the same array. The error word and the
 // combine counters are cleared on the call's stream before its kernel runs;
-// calls whose kernels overlap on the GPU (other streams, other host threads
-// without ordering) race on the array and give undefined results.
+// the decode kernel's counters start at zero (static storage) and every call
+// leaves them at zero (a call that recorded a device error may not). Calls
+// whose kernels overlap on the GPU (other streams, other host threads without
+// ordering) race on the array and give undefined results.
 
 #include <cstdint>
 #include <mutex>
@@ -29,8 +32,8 @@
 namespace moe {
 namespace {
 
-// 16 MiB: the combine staging of 142 tokens x top-8 x 7168 channels, and more than
-// any call without COMBINE needs (256 bytes).
+// 32 MiB: the decode partial tiles of 16-row blocks (7.9 MB) plus the combine staging
+// of 165 tokens x top-8 x 7168 channels; every call without COMBINE fits.
 constexpr size_t kStaticScratchBytes = MOE_W4A16_STATIC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
