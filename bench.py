@@ -547,10 +547,16 @@ def main(argv=None):
     dom = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    # keep the GPU under load while the clock sampler starts, so the timed steps do not begin
+    # on a GPU that idled (untimed steps, on top of the warm-up)
+    hot_until = time.perf_counter() + 0.2
+    while time.perf_counter() < hot_until:
+        for _ in range(4):
+            arm.step()
+        torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
-    sampler.start()
-    time.sleep(0.2)
     launches0 = M.launch_count()
     t0.record(stream)
     for i in range(args.steps):

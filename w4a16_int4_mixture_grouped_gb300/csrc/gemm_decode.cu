@@ -187,17 +187,22 @@ __device__ __forceinline__ bool piece_of(int64_t idx, int64_t U, int X, int KC, 
 
 // Part `part` of cut unit `su`: store this warp's FP32 partial tile; the warp that
 // brings the last part adds the parts in part order (deterministic) and returns true
-// to run the epilogue. Layout [su][part][warp][value][lane]. Not inlined: it runs
+// to run the epilogue. Layout [su][part][warp][value][lane]: a warp's load of one
+// value of a part is 32 consecutive floats; the sums run over batches of 8 values
+// with the loads of every part of a batch in flight at once. Not inlined: it runs
 // once per cut unit and keeps its registers out of the K loop.
 template <int ROWS>
 __device__ __noinline__ bool part_fixup(const GemmParams& p, int su, int part, int parts, int warp, int lane,
                                         float* acc) {
   constexpr int V = 2 * Geo<ROWS>::kTiles * 4;
-  auto slot = [&](int q) {
-    return p.sk_partials + ((static_cast<size_t>(su) * kParts + q) * kConsumerWarps + warp) * V * 32;
-  };
-  float* mine = slot(part);
-  for (int v = 0; v < V; ++v) mine[v * 32 + lane] = acc[v];
+  constexpr int kBatch = 8;
+  static_assert(V % kBatch == 0, "value batches");
+  constexpr size_t kPartStride = static_cast<size_t>(kConsumerWarps) * V * 32;
+  const float* base = p.sk_partials + (static_cast<size_t>(su) * kParts * kConsumerWarps + warp) * V * 32 + lane;
+  float* mine = p.sk_partials + (static_cast<size_t>(su) * kParts * kConsumerWarps + warp) * V * 32 + lane +
+                part * kPartStride;
+#pragma unroll
+  for (int v = 0; v < V; ++v) mine[v * 32] = acc[v];
   __threadfence();
   __syncwarp();
   int last = 0;
@@ -206,13 +211,21 @@ __device__ __noinline__ bool part_fixup(const GemmParams& p, int su, int part, i
   if (!last) return false;
   __threadfence();
   if (lane == 0) p.sk_counters[su * kConsumerWarps + warp] = 0;   // zero again for the next call
-  for (int v = 0; v < V; ++v) {
-    float sum = 0.f;
-    for (int q = 0; q < parts; ++q) {
-      const float y = q == part ? acc[v] : __ldcg(slot(q) + v * 32 + lane);
-      sum = q == 0 ? y : sum + y;
+#pragma unroll 1
+  for (int v0 = 0; v0 < V; v0 += kBatch) {
+    float sum[kBatch];
+#pragma unroll
+    for (int q = 0; q < kParts; ++q) {
+      if (q >= parts) break;
+      float y[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        y[j] = q == part ? acc[v0 + j] : __ldcg(base + q * kPartStride + (v0 + j) * 32);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) sum[j] = q == 0 ? y[j] : sum[j] + y[j];
     }
-    acc[v] = sum;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) acc[v0 + j] = sum[j];
   }
   return true;
 }

@@ -11,17 +11,43 @@ namespace moe {
 
 constexpr int kAlignCtas = 8;    // one thread-block cluster
 constexpr int kAlignWarps = 32;  // warps per CTA
+constexpr int kAlignBatch = 8;   // 32-row steps whose expert ids a lane loads at once
+static_assert(kAlignWarps * 32 >= MOE_W4A16_MAX_EXPERTS, "one thread per expert in the offset scan");
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Inclusive sum over the warp's lanes.
+__device__ __forceinline__ int warp_inclusive_sum(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
 
 // One cluster of kAlignCtas CTAs; CTA r takes a contiguous segment of the flat
-// routed rows f = t*top_k + j, split again over its warps:
-//  A. per-warp histograms of experts over the warp's rows (shared memory);
+// routed rows f = t*top_k + j, cut again into whole 32-row steps per warp (as
+// few warps as hold rows, up to kAlignWarps):
+//  A. per-warp histograms of experts over the warp's rows (shared memory), the
+//     ids of kAlignBatch steps loaded at once;
 //  B. per-(warp, expert) offsets within the CTA and the CTA's expert totals;
-//     every CTA then reads the other CTAs' totals through distributed shared
-//     memory: rows of each expert in earlier CTAs, and the expert totals;
-//  C. per-expert start offsets (padded to block_m, or e*max_m when masked);
+//     thread e then reads every CTA's total of expert e through distributed
+//     shared memory: rows of e in earlier CTAs, and e's total;
+//  C. per-expert start offsets (padded to block_m, or e*max_m when masked) by a
+//     block-wide scan, one expert per thread;
 //  D. each warp walks its rows in order, ranking equal experts within a
-//     32-row step with match.any, so rows land in ascending f per expert.
-// No global scratch: the cross-CTA exchange stays on chip.
+//     32-row step with match.any, so rows land in ascending f per expert;
+//  E. padding sentinels and the expert of every row block, experts spread
+//     over the cluster's warps.
+// No global scratch: the cross-CTA exchange stays on chip. A CTA signals that
+// it is done reading the others' shared memory right after B and waits for the
+// rest of the cluster only before it exits.
 __global__ void __cluster_dims__(kAlignCtas, 1, 1) __launch_bounds__(kAlignWarps * 32)
     align_kernel(const int32_t* __restrict__ ids, int R, int E, int block_m, int max_m,
                  int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids, int32_t* __restrict__ npp,
@@ -35,23 +61,37 @@ __global__ void __cluster_dims__(kAlignCtas, 1, 1) __launch_bounds__(kAlignWarps
   int* before = cta_cnt + E;             // [E] rows of each expert in earlier CTAs
   int* tot = before + E;                 // [E] rows of each expert
   int* start = tot + E;                  // [E + 1] padded start of each expert
+  __shared__ int wsum[kAlignWarps];
   const bool masked = max_m > 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
   const int cseg = (R + kAlignCtas - 1) / kAlignCtas;
   const int cbeg = min(R, rank * cseg), cend = min(R, cbeg + cseg);
-  const int wseg = (cend - cbeg + kAlignWarps - 1) / kAlignWarps;
-  const int beg = min(cend, cbeg + warp * wseg), end = min(cend, beg + wseg);
-  for (int i = beg + lane; i < end; i += 32) {
-    const int e = ids[i];
-    if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
-    else set_error(err, MOE_W4A16_ERR_BAD_INDEX);
+  const int steps = (cend - cbeg + 31) >> 5;
+  const int wsteps = (steps + kAlignWarps - 1) / kAlignWarps;
+  const int nw = wsteps > 0 ? (steps + wsteps - 1) / wsteps : 0;   // warps holding rows
+  const int beg = min(cend, cbeg + warp * wsteps * 32), end = min(cend, beg + wsteps * 32);
+  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int b0 = beg; b0 < end; b0 += 32 * kAlignBatch) {
+    int ev[kAlignBatch];
+#pragma unroll
+    for (int j = 0; j < kAlignBatch; ++j) {
+      const int i = b0 + 32 * j + lane;
+      ev[j] = i < end ? ids[i] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kAlignBatch; ++j) {
+      if (b0 + 32 * j + lane >= end) break;
+      const int e = ev[j];
+      if (e >= 0 && e < E) atomicAdd(&hist[warp * E + e], 1);
+      else set_error(err, MOE_W4A16_ERR_BAD_INDEX);
+    }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  const int e = threadIdx.x;             // this thread's expert in B and C
+  if (e < E) {
     int c = 0;
-    for (int w = 0; w < kAlignWarps; ++w) {
+    for (int w = 0; w < nw; ++w) {
       const int h = hist[w * E + e];
       hist[w * E + e] = c;
       c += h;
@@ -59,12 +99,16 @@ __global__ void __cluster_dims__(kAlignCtas, 1, 1) __launch_bounds__(kAlignWarps
     cta_cnt[e] = c;
   }
   cluster.sync();   // every CTA's totals are final
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int b = 0, t = 0;
+  int t = 0;
+  if (e < E) {
+    int cnt[kAlignCtas];
+#pragma unroll
+    for (int r = 0; r < kAlignCtas; ++r) cnt[r] = *cluster.map_shared_rank(cta_cnt + e, r);
+    int b = 0;
+#pragma unroll
     for (int r = 0; r < kAlignCtas; ++r) {
-      const int c = *cluster.map_shared_rank(cta_cnt + e, r);
-      if (r < rank) b += c;
-      t += c;
+      if (r < rank) b += cnt[r];
+      t += cnt[r];
     }
     before[e] = b;
     tot[e] = t;
@@ -73,58 +117,63 @@ __global__ void __cluster_dims__(kAlignCtas, 1, 1) __launch_bounds__(kAlignWarps
       if (masked && t > max_m) set_error(err, MOE_W4A16_ERR_CAPACITY);
     }
   }
+  cluster_arrive_release();   // done with the other CTAs' shared memory
+  const int padded = e < E ? (masked ? max_m : ((t + block_m - 1) / block_m) * block_m) : 0;
+  const int incl = warp_inclusive_sum(padded, lane);
+  if (lane == 31) wsum[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    int carry = 0;
-    for (int b0 = 0; b0 < E; b0 += 32) {
-      const int e = b0 + lane;
-      int padded = 0;
-      if (e < E) padded = masked ? max_m : ((tot[e] + block_m - 1) / block_m) * block_m;
-      int v = padded;
+  if (warp == 0) wsum[lane] = warp_inclusive_sum(wsum[lane], lane);
+  __syncthreads();
+  if (e < E) {
+    const int excl = incl - padded + (warp > 0 ? wsum[warp - 1] : 0);
+    start[e] = excl;
+    if (e == E - 1) {
+      start[E] = excl + padded;
+      if (!masked && rank == 0) *npp = excl + padded;
+    }
+  }
+  __syncthreads();
+  for (int b0 = beg; b0 < end; b0 += 32 * kAlignBatch) {
+    int ev[kAlignBatch];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
-      }
-      if (e < E) start[e] = carry + v - padded;
-      carry += __shfl_sync(0xffffffffu, v, 31);
+    for (int j = 0; j < kAlignBatch; ++j) {
+      const int i = b0 + 32 * j + lane;
+      ev[j] = i < end ? ids[i] : -1;
     }
-    if (lane == 0) start[E] = carry;
-  }
-  __syncthreads();
-  for (int b0 = beg; b0 < end; b0 += 32) {
-    const int i = b0 + lane;
-    const int e = i < end ? ids[i] : -1;
-    const bool valid = e >= 0 && e < E;
-    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
-    const int rk = __popc(peers & ((1u << lane) - 1u));
-    int off = 0;
-    if (valid) off = before[e] + hist[warp * E + e] + rk;
-    __syncwarp();
-    if (valid) {
-      if (lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
-      if (masked) {
-        if (off < max_m) masked_rows[start[e] + off] = i;
-      } else {
-        sorted_ids[start[e] + off] = i;
+#pragma unroll
+    for (int j = 0; j < kAlignBatch; ++j) {
+      if (b0 + 32 * j >= end) break;       // warp-uniform
+      const int i = b0 + 32 * j + lane;
+      const int x = ev[j];
+      const bool valid = i < end && x >= 0 && x < E;
+      const unsigned peers = __match_any_sync(0xffffffffu, valid ? x : E + lane);
+      const int rk = __popc(peers & ((1u << lane) - 1u));
+      int off = 0;
+      if (valid) off = before[x] + hist[warp * E + x] + rk;
+      __syncwarp();
+      if (valid) {
+        if (lane == __ffs(peers) - 1) hist[warp * E + x] += __popc(peers);
+        if (masked) {
+          if (off < max_m) masked_rows[start[x] + off] = i;
+        } else {
+          sorted_ids[start[x] + off] = i;
+        }
       }
+      __syncwarp();
     }
-    __syncwarp();
   }
-  // padding: sentinels / -1 fill and the expert of every block (experts split over the cluster)
-  for (int e = rank + kAlignCtas * warp; e < E; e += kAlignCtas * kAlignWarps) {
-    const int c = masked ? min(tot[e], max_m) : tot[e];
-    const int s0 = start[e], s_end = start[e + 1];
+  for (int x = rank + kAlignCtas * warp; x < E; x += kAlignCtas * kAlignWarps) {
+    const int c = masked ? min(tot[x], max_m) : tot[x];
+    const int s0 = start[x], s_end = start[x + 1];
     for (int pos = s0 + c + lane; pos < s_end; pos += 32) {
       if (masked) masked_rows[pos] = -1;
       else sorted_ids[pos] = R;
     }
     if (!masked) {
-      for (int b = s0 / block_m + lane; b < s_end / block_m; b += 32) expert_ids[b] = e;
+      for (int b = s0 / block_m + lane; b < s_end / block_m; b += 32) expert_ids[b] = x;
     }
   }
-  if (!masked && rank == 0 && threadIdx.x == 0) *npp = start[E];
-  cluster.sync();   // no CTA leaves while another may still read its shared memory
+  cluster_wait_acquire();     // no CTA leaves while another may still read its shared memory
 }
 
 __global__ void contiguous_layout_kernel(const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ expert_ids,
