@@ -107,7 +107,7 @@ enum {
 #define MOE_W4A16_VERSION 1u
 #define MOE_W4A16_MAX_EXPERTS 1024
 #define MOE_W4A16_WS_HEADER_BYTES 256
-#define MOE_W4A16_STATIC_SCRATCH_BYTES (32u << 20) /* scratch of moe_w4a16_indexed_noalloc */
+#define MOE_W4A16_STATIC_SCRATCH_BYTES (48u << 20) /* scratch of moe_w4a16_indexed_noalloc */
 
 /* Host-side description of a prepared weight, filled by moe_w4a16_prepare and
  * passed by address to every GEMM call (host pointer). */
@@ -258,10 +258,10 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int to
  * GEMM reads consecutive rows; for MOE_W4A16_FLAG_COMBINE an arrival counter
  * per (token, 256 output channels, slice) and a bf16 [num_tokens*top_k, n]
  * staging buffer for the routed rows; for calls that may run the decode kernel
- * (indexed block_m <= 32, masked) with n <= 1024, the FP32 partial tiles and
- * counters of the units it cuts into k-ranges when a call has at most 120
- * (row block, 256-channel) units (120 units x 4 parts: 7.9 MB for
- * block_m <= 16, 15.7 MB for 32-row blocks and masked calls).
+ * (indexed block_m <= 32, masked), the FP32 partial tiles and counters of the
+ * units it cuts into k-ranges: the last min(units, 152) units of a call with
+ * at most 2048 (row block, 256-channel) units (152 units x 4 parts: 10.0 MB for
+ * block_m <= 16, 19.9 MB for 32-row blocks and masked calls).
  * block_m is ignored for the other grouped layout. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_workspace_size(int layout, int num_tokens, int top_k, int num_experts, int n,
                                                         int k, int block_m, uint32_t flags, size_t* bytes);
@@ -318,14 +318,14 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad
  * It computes exactly what moe_w4a16_indexed computes for block_m 1..32, with
  * the same arguments except the workspace, and takes its scratch (device error
  * word, combine counters, combine staging rows, decode partial tiles) from one statically reserved
- * device array of MOE_W4A16_STATIC_SCRATCH_BYTES (32 MiB) per device.
+ * device array of MOE_W4A16_STATIC_SCRATCH_BYTES (48 MiB) per device.
  *   block_m    1..32 (decode kernel only), else INVALID_ARG
  *   scratch    optional host pointer; receives the device address of the array,
  *              whose first int32 is this call's device error word (read it with
  *              moe_w4a16_get_device_error). Owned by the library: never free it.
  * A call whose moe_w4a16_workspace_size exceeds MOE_W4A16_STATIC_SCRATCH_BYTES
- * (with n <= 1024: 7.9 MB of decode partial tiles at block_m <= 16, 15.7 MB
- * above; with COMBINE also 2*num_tokens*top_k*n bytes of staging) returns
+ * (10.0 MB of decode partial tiles at block_m <= 16, 19.9 MB above; with
+ * COMBINE also 2*num_tokens*top_k*n bytes of staging) returns
  * MOE_W4A16_ERR_SCRATCH_LIMIT before any CUDA call. No cudaMalloc, cudaFree or
  * allocating library routine is called.
  * Set-up: the first call on a device, with that device current, resolves the

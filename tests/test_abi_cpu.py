@@ -74,25 +74,23 @@ def test_align_size_capacity(lib):
 def test_workspace_size(lib):
     out = ctypes.c_size_t(0)
     f = lib.moe_w4a16_workspace_size
-    # masked / decode-family indexed calls: header only
-    assert f(2, 128, 8, 384, 7168, 2048, 0, 0, ctypes.byref(out)) == 0 and out.value == 256
-    assert f(0, 128, 8, 384, 7168, 2048, 32, 0, ctypes.byref(out)) == 0 and out.value == 256
-    # narrow outputs (n <= 1024) on the decode kernel: + the partial tiles of units cut into 4 k-ranges when
-    # a call has at most 120 units (120 units x 4 parts x 8 warps x 32 lanes x FP32 values: 16 for 16-row
-    # blocks, 32 for 32-row blocks and masked calls) + their counters
-    cut16 = 120 * 4 * 8 * 16 * 32 * 4 + 120 * 8 * 4
-    cut32 = 120 * 4 * 8 * 32 * 32 * 4 + 120 * 8 * 4
-    assert f(0, 64, 8, 384, 512, 7168, 16, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut16
-    assert f(0, 64, 8, 384, 1024, 7168, 32, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut32
-    assert f(2, 64, 8, 384, 512, 7168, 0, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut32
-    assert f(0, 64, 8, 384, 1280, 7168, 16, 0, ctypes.byref(out)) == 0 and out.value == 256
+    # decode-family calls (masked, indexed block_m <= 32): header + the partial tiles of the units the kernel
+    # cuts into 4 k-ranges (the last 152 units of a call with at most 2048 units: 152 units x 4 parts x 8
+    # warps x 32 lanes x FP32 values, 16 for 16-row blocks, 32 for 32-row blocks and masked calls) + their
+    # arrival counters (152 x 8 int32)
+    cut16 = 152 * 4 * 8 * 16 * 32 * 4 + 152 * 8 * 4
+    cut32 = 152 * 4 * 8 * 32 * 32 * 4 + 152 * 8 * 4
+    assert f(2, 128, 8, 384, 7168, 2048, 0, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut32
+    assert f(0, 128, 8, 384, 7168, 2048, 32, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut32
+    assert f(0, 64, 8, 384, 4096, 7168, 16, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut16
+    assert f(0, 64, 8, 384, 512, 7168, 1, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut16
     cap = 64 * 8 + 384 * 63                         # tcgen05 block sizes: gathered rows, no partial tiles
     assert f(0, 64, 8, 384, 512, 7168, 64, 0, ctypes.byref(out)) == 0 and out.value == 256 + cap * 7168 * 2
     # combine: arrival counters + routed-row staging
     assert f(0, 128, 8, 384, 7168, 2048, 32, 2 | 4, ctypes.byref(out)) == 0
     counters = -(-(128 * 28 * 8 * 4) // 256) * 256
     y = -(-(1024 * 7168 * 2) // 256) * 256
-    assert out.value == 256 + counters + y
+    assert out.value == 256 + counters + y + cut32
     # indexed on the tcgen05 family: + gathered activations [max_sorted, K]
     cap = 8192 * 8 + 384 * 255
     cap = -(-cap // 256) * 256
@@ -154,14 +152,14 @@ def test_gemm_host_checks_reject_before_launch(lib):
 
 
 def test_noalloc_rejects_before_any_cuda_call(lib):
-    """The static-scratch entry point refuses calls whose scratch exceeds 32 MiB, and prefill block sizes."""
+    """The static-scratch entry point refuses calls whose scratch exceeds 48 MiB, and prefill block sizes."""
     d = _desc(e=4, n=1024, k=64)
 
     def call(t, k, block_m, flags, desc=d):
         return lib.moe_w4a16_indexed_noalloc(FAKE, t * k, 64, ctypes.byref(desc) if desc else None, FAKE, FAKE, FAKE, FAKE, t, k, block_m, FAKE,
                                              ctypes.c_uint32(flags), FAKE, None, None)
 
-    assert call(2000, 8, 16, 2 | 4) == 9              # counters + 2000*8*1024*2 B + partial tiles > 32 MiB
+    assert call(3200, 8, 16, 2 | 4) == 9              # counters + 3200*8*1024*2 B + partial tiles > 48 MiB
     assert call(8, 8, 64, 0) == 1                     # block_m above 32 runs the prefill kernel: refused
     assert call(8, 8, 0, 0) == 1
     assert call(8, 8, 16, 0, desc=None) == 1

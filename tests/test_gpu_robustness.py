@@ -1,9 +1,10 @@
 """Run-to-run determinism and workspace reuse.
 
-The decode kernel hands units out on demand and cuts nothing, so which CTA
-computes a unit changes from run to run while every output must not: each
-unit's sums run in a fixed order and the combine adds a token's rows in slot
-order. Every counter in a workspace is back at zero after a call, so one
+The decode kernel hands units (and, at the end of small calls, k-range parts
+of units) out on demand, so which CTA computes a unit changes from run to run
+while every output must not: each unit's sums run in a fixed order, the parts
+of a cut unit are added in part order, and the combine adds a token's rows in
+slot order. Every counter in a workspace is back at zero after a call, so one
 workspace serves calls of different shapes, also after a call that recorded a
 device error and had its error word cleared.
 """

@@ -194,10 +194,8 @@ struct WsLayout {
 };
 
 // Rows per block for which the decode kernel's cut-unit partial tiles are sized (0: the call does
-// not run the decode kernel with cut units: prefill block sizes, or an output wider than
-// kCutMaxGroups groups). Masked row budgets are not known here: 32-row size.
-static int cut_rows(int layout, int block_m, int n) {
-  if (n > kCutMaxGroups * kGroupN) return 0;
+// not run the decode kernel). Masked row budgets are not known here: 32-row size.
+static int cut_rows(int layout, int block_m) {
   if (layout == MOE_W4A16_LAYOUT_MASKED) return kDecodeRows;
   if (layout != MOE_W4A16_LAYOUT_INDEXED || block_m < 1 || block_m > kDecodeRows) return 0;
   return block_m <= kDecodeRowsSmall ? kDecodeRowsSmall : kDecodeRows;
@@ -240,7 +238,7 @@ static moe_w4a16_status ws_layout(int layout, int num_tokens, int top_k, int num
     L->cb_off = off;
     off += align_up((static_cast<size_t>(L->cb_segs) + 1) * 16, 256);
   }
-  if (const int rows = cut_rows(layout, block_m, n)) {
+  if (const int rows = cut_rows(layout, block_m)) {
     L->cut_off = off;
     L->cut_bytes = cut_partial_bytes(rows);
     off += L->cut_bytes;

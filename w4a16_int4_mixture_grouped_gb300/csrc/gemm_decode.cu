@@ -44,9 +44,16 @@ constexpr int kActStride = 144;                         // 128 B of k + 16 B pad
 #define MOE_W4A16_DECODE_STAGES 6
 #endif
 constexpr int kStages = MOE_W4A16_DECODE_STAGES;
-constexpr int kMiscBytes = 256;                         // barriers, abort flag, stage descriptors
-constexpr int kDescOffset = 160;                        // int per stage inside the misc area
-static_assert(2 * kStages * 8 + 4 <= kDescOffset && kDescOffset + 4 * kStages <= kMiscBytes, "misc area layout");
+constexpr int kMiscBytes = 256;                         // barriers, abort flag
+static_assert(2 * kStages * 8 + 4 <= kMiscBytes, "misc area layout");
+// Piece record, one per stage, written by the producer into the first stage of each
+// piece it hands to the consumers: the piece, its 256-channel group, its k-chunk count,
+// its part (-1: whole unit) and cut-unit index, its 8-row token tiles, then per row of
+// the block the A row and the output row (the flat routed-row id for the combine).
+// Consumers take a piece from it without touching the routing arrays in global memory.
+enum { kRecIdx = 0, kRecGroup, kRecChunks, kRecPart, kRecCut, kRecTiles, kRecMeta = 8 };
+constexpr int kRecInts = kRecMeta + 2 * 32;
+constexpr int kRecBytes = kStages * kRecInts * 4;
 constexpr int kSlices = kConsumerWarps;                 // combine counter slices per group
 
 // Geometry of the kernel variant whose row blocks hold up to ROWS (16 or 32)
@@ -61,7 +68,9 @@ struct Geo {
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kCtasPerSm = ROWS == 16 ? 3 : 2;
   static constexpr int kRowIters = ROWS / 4;                           // activation pieces per producer lane
-  static constexpr int smem_bytes(int prefix_entries) { return kBarOffset + kMiscBytes + prefix_entries * 4; }
+  static constexpr int kRecOffset = kBarOffset + kMiscBytes;
+  static constexpr int kPrefixOffset = kRecOffset + kRecBytes;
+  static constexpr int smem_bytes(int prefix_entries) { return kPrefixOffset + prefix_entries * 4; }
 };
 
 #ifdef MOE_W4A16_PIPE_STATS
@@ -87,7 +96,7 @@ __device__ __forceinline__ void store_bf16(uint16_t* base, int64_t idx, float v)
 // stage, a lane loads its four FU words of each chunk, its scales, and the
 // activation B fragments of NT tiles, releases the stage, then dequantises
 // 8 FUs and issues 8*NT MMAs. Returns false when a wait gave up.
-template <int ROWS, int NT, bool CUT>
+template <int ROWS, int NT>
 __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s, int& stage, uint32_t& phase,
                                              uint32_t wq_off, uint32_t sc_off, int lane, int nkc,
                                              float (&acc)[2][Geo<ROWS>::kTiles][4], PipeStats& ps) {
@@ -98,8 +107,7 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
   const uint32_t act_lane = 2 * kChunkBytes + (lane & 7) * kActStride + (lane >> 3) * 16;
-  const int kcs = CUT ? nkc : p.KC;   // the uncut variant reads K-chunks from the parameters
-  for (int kc = 0; kc < kcs; ++kc) {
+  for (int kc = 0; kc < nkc; ++kc) {
     ps.start();
     if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) return false;
     ps.stop(0);
@@ -147,21 +155,24 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
   return true;
 }
 
-// Pieces handed out by the unit counter: whole units in order, except that a call
-// with a narrow output (at most kCutMaxGroups 256-channel groups, e.g. one
-// tensor-parallel shard) and at most kMaxCutUnits units has every unit cut into
-// kParts k-ranges so that more CTAs stream weights. The Chord page (section "H200
-// prefill and TP8") gives TP8 its own flatter tiling for the same reason: a narrow
-// intermediate leaves few N tiles per SM. A cut unit is summed by the last of its
-// parts to arrive, parts in order. The choice depends on N and the unit count
-// alone, not on the grid, so a call's result does not depend on how it was launched.
+// Pieces handed out by the unit counter: whole units in order, then, in a call with
+// at most kCutUnitLimit units, its last min(units, kMaxCutUnits) units cut into
+// kParts k-ranges each. With a few units per SM the SMs that take one unit more than
+// the others set the end (measured: 8 of 152 SMs ran a sixth 56 us unit of the
+// 768-unit decode gate_up); quarter units at the end even them out. A call with
+// fewer units than SMs (a narrow output such as one tensor-parallel shard's gate_up;
+// the Chord page, section "H200 prefill and TP8", tiles TP8 more flatly for the same
+// reason) has every unit cut, so that more CTAs stream weights. A cut unit is summed
+// by the last of its parts to arrive, parts in order. The choice depends on the unit
+// count alone, not on the grid, so a call's result does not depend on how it was
+// launched.
 struct Piece {
   int u, kc0, kc1, part;  // part -1: a whole unit
 };
 
 __device__ __forceinline__ int split_units(int64_t U, const GemmParams& p) {
-  if (p.sk_partials == nullptr || U > p.sk_units) return 0;
-  return static_cast<int>(U);
+  if (p.sk_partials == nullptr || U > kCutUnitLimit) return 0;
+  return static_cast<int>(U < p.sk_units ? U : p.sk_units);
 }
 
 // Piece `idx` of a call with U units of KC k-chunks and X cut units (false: none left).
@@ -185,24 +196,27 @@ __device__ __forceinline__ bool piece_of(int64_t idx, int64_t U, int X, int KC, 
   return true;
 }
 
-// Part `part` of cut unit `su`: store this warp's FP32 partial tile; the warp that
-// brings the last part adds the parts in part order (deterministic) and returns true
+// Part `part` of cut unit `su`: every part stores this warp's FP32 partial tile; the
+// warp that brings the last part loads the parts back and adds them in part order
+// (deterministic), one part's values in flight at a time, into acc, and returns true
 // to run the epilogue. Layout [su][part][warp][value][lane]: a warp's load of one
-// value of a part is 32 consecutive floats; the sums run over batches of 8 values
-// with the loads of every part of a batch in flight at once. Not inlined: it runs
-// once per cut unit and keeps its registers out of the K loop.
+// value of a part is 32 consecutive floats.
 template <int ROWS>
-__device__ __noinline__ bool part_fixup(const GemmParams& p, int su, int part, int parts, int warp, int lane,
-                                        float* acc) {
-  constexpr int V = 2 * Geo<ROWS>::kTiles * 4;
-  constexpr int kBatch = 8;
-  static_assert(V % kBatch == 0, "value batches");
+__device__ __forceinline__ bool part_fixup(const GemmParams& p, int su, int part, int parts, int warp, int lane,
+                                           float (&acc)[2][Geo<ROWS>::kTiles][4]) {
+  constexpr int T = Geo<ROWS>::kTiles;
+  constexpr int V = 2 * T * 4;
   constexpr size_t kPartStride = static_cast<size_t>(kConsumerWarps) * V * 32;
-  const float* base = p.sk_partials + (static_cast<size_t>(su) * kParts * kConsumerWarps + warp) * V * 32 + lane;
-  float* mine = p.sk_partials + (static_cast<size_t>(su) * kParts * kConsumerWarps + warp) * V * 32 + lane +
-                part * kPartStride;
+  float* base = p.sk_partials + (static_cast<size_t>(su) * kParts * kConsumerWarps + warp) * V * 32 + lane;
+  {
+    float* mine = base + part * kPartStride;
 #pragma unroll
-  for (int v = 0; v < V; ++v) mine[v * 32] = acc[v];
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int nt = 0; nt < T; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mine[((c * T + nt) * 4 + i) * 32] = acc[c][nt][i];
+  }
   __threadfence();
   __syncwarp();
   int last = 0;
@@ -212,25 +226,22 @@ __device__ __noinline__ bool part_fixup(const GemmParams& p, int su, int part, i
   __threadfence();
   if (lane == 0) p.sk_counters[su * kConsumerWarps + warp] = 0;   // zero again for the next call
 #pragma unroll 1
-  for (int v0 = 0; v0 < V; v0 += kBatch) {
-    float sum[kBatch];
+  for (int q = 0; q < parts; ++q) {
+    const float* src = base + q * kPartStride;
 #pragma unroll
-    for (int q = 0; q < kParts; ++q) {
-      if (q >= parts) break;
-      float y[kBatch];
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j)
-        y[j] = q == part ? acc[v0 + j] : __ldcg(base + q * kPartStride + (v0 + j) * 32);
+      for (int nt = 0; nt < T; ++nt)
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) sum[j] = q == 0 ? y[j] : sum[j] + y[j];
-    }
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) acc[v0 + j] = sum[j];
+        for (int i = 0; i < 4; ++i) {
+          const float y = __ldcg(src + ((c * T + nt) * 4 + i) * 32);
+          acc[c][nt][i] = q == 0 ? y : acc[c][nt][i] + y;
+        }
   }
   return true;
 }
 
-template <int ROWS, bool CUT>
+template <int ROWS>
 __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_kernel(const GemmParams p) {
   using G = Geo<ROWS>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -239,9 +250,8 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
   s.full = smem_u32(smem + G::kBarOffset);
   s.empty = s.full + kStages * 8;
   s.abort_flag = reinterpret_cast<volatile int*>(smem + G::kBarOffset + 2 * kStages * 8);
-  s.prefix = reinterpret_cast<int*>(smem + G::kBarOffset + kMiscBytes);
-  // unit of the piece that starts at each stage (-1: no more work), written by the producer
-  volatile int* desc = reinterpret_cast<volatile int*>(smem + G::kBarOffset + kDescOffset);
+  s.prefix = reinterpret_cast<int*>(smem + G::kPrefixOffset);
+  int* recs = reinterpret_cast<int*>(smem + G::kRecOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -266,18 +276,16 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     uint32_t phase = 0;
     bool issued_any = false;
     PipeStats pps;
-    const int X = CUT ? split_units(total_units, p) : 0;
+    const int X = split_units(total_units, p);
     while (true) {
       // pieces are handed out in order, one at a time, to whichever CTA asks next
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.grab, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
-      Piece pc{idx, 0, p.KC, -1};
-      if (CUT ? !piece_of(idx, total_units, X, p.KC, pc) : idx >= total_units) break;
+      Piece pc;
+      if (!piece_of(idx, total_units, X, p.KC, pc)) break;
       const int u = pc.u;
-      // (the uncut variant divides in 64 bits: with it ptxas allocates that kernel without spills)
-      const int blk = CUT ? u / p.NG : static_cast<int>(static_cast<int64_t>(u) / p.NG);
-      const int gp = CUT ? u % p.NG : static_cast<int>(static_cast<int64_t>(u) % p.NG);
+      const int blk = u / p.NG, gp = u % p.NG;
       int local;
       const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
       if (e < 0) continue;
@@ -285,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       const bool valid = rr.a_row >= 0;
       const unsigned vmask = __ballot_sync(0xffffffffu, valid);
       if (vmask == 0) continue;
+      const int orow = (p.flags & MOE_W4A16_FLAG_COMBINE) ? rr.flat : rr.out_row;
       const uint8_t* wsrc = p.chunks + group_offset(e, gp, p.NB, p.KC);
       // activation rows by cp.async: lane copies 16-byte piece (lane & 7) of rows (lane >> 3) + 4j
       const uint16_t* asrc[G::kRowIters];
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
         asrc[j] = ar >= 0 ? p.a + static_cast<int64_t>(ar) * p.K + (lane & 7) * 8 : nullptr;
       }
       const uint32_t adst = 2 * kChunkBytes + (lane >> 3) * kActStride + (lane & 7) * 16;
-      const int kc0 = CUT ? pc.kc0 : 0, kc1 = CUT ? pc.kc1 : p.KC;
+      const int kc0 = pc.kc0, kc1 = pc.kc1;
       for (int kc = kc0; kc < kc1; ++kc) {
         pps.start();
         if (!warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err)) goto producer_done;
@@ -303,8 +312,22 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
         pps.add(1, 1);
         const uint32_t full = s.full + 8 * stage;
         const uint32_t sb = s.stages + stage * G::kStageBytes;
+        if (kc == kc0) {
+          // the piece record; lane 0's arrive below publishes it with the stage
+          int* rec = recs + stage * kRecInts;
+          rec[kRecMeta + lane] = rr.a_row;
+          rec[kRecMeta + 32 + lane] = orow;
+          if (lane == 0) {
+            rec[kRecIdx] = idx;
+            rec[kRecGroup] = gp;
+            rec[kRecChunks] = kc1 - kc0;
+            rec[kRecPart] = pc.part;
+            rec[kRecCut] = pc.part >= 0 ? u - static_cast<int>(total_units - X) : 0;
+            rec[kRecTiles] = (32 - __clz(vmask) + 7) >> 3;
+          }
+          __syncwarp();
+        }
         if (lane == 0) {
-          if (kc == kc0) desc[stage] = idx;
           mbar_arrive_expect_tx(full, kPairBytes);
           bulk_g2s_hint(sb, wsrc + static_cast<size_t>(kc) * kPairBytes, kPairBytes, full, pol);
         }
@@ -322,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     // no more units: one stage carries the end mark (33 plain arrivals complete its phase)
     if (warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err)) {
       if (lane == 0) {
-        desc[stage] = -1;
+        recs[stage * kRecInts + kRecIdx] = -1;
         mbar_arrive(s.full + 8 * stage);
       }
       __syncwarp();
@@ -351,53 +374,35 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     const uint32_t wq_off = (warp * 32 + lane) * 16;
     const uint32_t sc_off = kChunkWBytes + (warp * 8 + g) * 8;
     PipeStats cps;
-    const int X = CUT ? split_units(total_units, p) : 0;
     while (true) {
       cps.stop(3);   // epilogue of the previous unit (and unit bookkeeping)
       // the next piece is the one the producer put at the head of the current stage
       if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) goto consumer_done;
-      const int idx = desc[stage];
-      Piece pc{idx, 0, p.KC, -1};
-      if (idx < 0 || (CUT && !piece_of(idx, total_units, X, p.KC, pc))) break;
-      const int u = pc.u;
-      const int blk = u / p.NG, gp = u % p.NG;
-      int local;
-      const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
-      if (e < 0) break;   // never: the producer hands out only units with work
-      const RowRef rr = block_row(p, blk, e, local, rows_per_block, lane);
-      const unsigned vmask = __ballot_sync(0xffffffffu, rr.a_row >= 0);
-      if (vmask == 0) break;
-      const int ntiles = (32 - __clz(vmask) + 7) >> 3;
+      const int* rec = recs + stage * kRecInts;
+      if (rec[kRecIdx] < 0) break;
+      const int gp = rec[kRecGroup], ntiles = rec[kRecTiles];
+      const int a_row = rec[kRecMeta + lane], orow = rec[kRecMeta + 32 + lane];
+      const int nkc = rec[kRecChunks], part = rec[kRecPart], cut_unit = rec[kRecCut];
 
       float acc[2][G::kTiles][4];
-      const int nkc = pc.kc1 - pc.kc0;
       bool ok;
       cps.start();
       const long long t_unit = clock64();
       switch (ntiles) {
-        case 1: ok = consume_unit<ROWS, 1, CUT>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
-        case 2: ok = consume_unit<ROWS, 2, CUT>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
+        case 1: ok = consume_unit<ROWS, 1>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
+        case 2: ok = consume_unit<ROWS, 2>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
         case 3:
-          ok = consume_unit<ROWS, (G::kTiles > 2 ? 3 : 2), CUT>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps);
+          ok = consume_unit<ROWS, (G::kTiles > 2 ? 3 : 2)>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps);
           break;
-        default: ok = consume_unit<ROWS, G::kTiles, CUT>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
+        default: ok = consume_unit<ROWS, G::kTiles>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
       }
       cps.add(2, static_cast<unsigned long long>(clock64() - t_unit));
       cps.add(4, 1);
       cps.start();
       if (!ok) goto consumer_done;
-      if (CUT && pc.part >= 0) {
-        // a cut unit: only the last of its parts runs the epilogue
-        constexpr int V = 2 * G::kTiles * 4;
-        float part[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) part[v] = acc[v / (4 * G::kTiles)][(v / 4) % G::kTiles][v % 4];
-        if (!part_fixup<ROWS>(p, u - static_cast<int>(total_units - X), pc.part, p.KC < kParts ? p.KC : kParts, warp,
-                              lane, part))
-          continue;
-#pragma unroll
-        for (int v = 0; v < V; ++v) acc[v / (4 * G::kTiles)][(v / 4) % G::kTiles][v % 4] = part[v];
-      }
+      // a cut unit: only the last of its parts runs the epilogue
+      if (part >= 0 && !part_fixup<ROWS>(p, cut_unit, part, p.KC < kParts ? p.KC : kParts, warp, lane, acc))
+        continue;
 
       // ---------------------------------------------------------- epilogue
       // acc[c][nt]: channels ch = c*128 + warp*16 + g (+8), token slots nt*8 + 2t (+1)
@@ -411,8 +416,8 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int slot = nt * 8 + 2 * t + j;
-            const int out_row = __shfl_sync(0xffffffffu, combine ? rr.flat : rr.out_row, slot);
-            const int a_ok = __shfl_sync(0xffffffffu, rr.a_row, slot);
+            const int out_row = __shfl_sync(0xffffffffu, orow, slot);
+            const int a_ok = __shfl_sync(0xffffffffu, a_row, slot);
             if (a_ok < 0 || out_row < 0) continue;
             const float v00 = acc[0][nt][j], v08 = acc[0][nt][2 + j];
             const float v10 = acc[1][nt][j], v18 = acc[1][nt][2 + j];
@@ -446,8 +451,8 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
           __syncwarp();
           int tok = -1;
           bool last = false;
-          if (rr.a_row >= 0 && rr.flat >= 0) {
-            tok = rr.flat / p.top_k;
+          if (a_row >= 0 && orow >= 0) {
+            tok = orow / p.top_k;
             last = atomicAdd(combine_counter(p, tok, gp, warp, kSlices), 1) == p.top_k - 1;
           }
           unsigned lm = __ballot_sync(0xffffffffu, last);
@@ -487,14 +492,14 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
 
 namespace decode {
 
-template <int ROWS, bool CUT>
+template <int ROWS>
 cudaError_t launch_rows(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
   using G = Geo<ROWS>;
   const DeviceInfo& di = device_info(device);
   const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
   static bool attr_set[64] = {false};
   if (device >= 0 && device < 64 && !attr_set[device]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<ROWS, CUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          G::smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
     if (e != cudaSuccess) return e;
     attr_set[device] = true;
@@ -508,7 +513,7 @@ cudaError_t launch_rows(const GemmParams& p, int device, cudaStream_t stream, in
   int64_t grid = static_cast<int64_t>(di.sm_count) * G::kCtasPerSm;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  decode_gemm_kernel<ROWS, CUT><<<static_cast<int>(grid), kThreads, G::smem_bytes(prefix_entries), stream>>>(p);
+  decode_gemm_kernel<ROWS><<<static_cast<int>(grid), kThreads, G::smem_bytes(prefix_entries), stream>>>(p);
   note_launch();
   if (grid_out) *grid_out = static_cast<int>(grid);
   return cudaGetLastError();
@@ -517,19 +522,12 @@ cudaError_t launch_rows(const GemmParams& p, int device, cudaStream_t stream, in
 }  // namespace decode
 
 // Row blocks of at most 16 rows (indexed block_m <= 16, masked budget <= 16) run
-// the 16-row variant; contiguous blocks and larger ones the 32-row variant. Narrow
-// outputs (at most kCutMaxGroups 256-channel groups, e.g. a tensor-parallel shard's
-// gate_up) run the variant that may cut units into k-ranges; the others keep a K
-// loop without that bookkeeping (its registers cost 3-4% on the wide shapes).
+// the 16-row variant; contiguous blocks and larger ones the 32-row variant.
 cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
   const bool small = (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.block_m <= kDecodeRowsSmall) ||
                      (p.layout == MOE_W4A16_LAYOUT_MASKED && p.max_m <= kDecodeRowsSmall);
-  const bool cut = p.sk_partials != nullptr && p.NG <= kCutMaxGroups;
-  if (small)
-    return cut ? decode::launch_rows<kDecodeRowsSmall, true>(p, device, stream, grid_out)
-               : decode::launch_rows<kDecodeRowsSmall, false>(p, device, stream, grid_out);
-  return cut ? decode::launch_rows<kDecodeRows, true>(p, device, stream, grid_out)
-             : decode::launch_rows<kDecodeRows, false>(p, device, stream, grid_out);
+  return small ? decode::launch_rows<kDecodeRowsSmall>(p, device, stream, grid_out)
+               : decode::launch_rows<kDecodeRows>(p, device, stream, grid_out);
 }
 
 }  // namespace moe

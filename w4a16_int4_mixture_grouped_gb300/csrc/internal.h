@@ -123,11 +123,11 @@ cudaError_t launch_combine_rows(const uint16_t* y, const float* w, int T, int to
 cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out);
 cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out);
 
-// Decode: a call with at most kCutMaxGroups 256-channel groups and at most kMaxCutUnits
-// units has every unit cut into kParts k-ranges.
+// Decode: a call with at most kCutUnitLimit (row block, 256-channel group) units has its
+// last min(units, kMaxCutUnits) units cut into kParts k-ranges.
 constexpr int kParts = 4;
-constexpr int kMaxCutUnits = 120;
-constexpr int kCutMaxGroups = 4;
+constexpr int kMaxCutUnits = 152;
+constexpr int kCutUnitLimit = 2048;
 // Bytes of the cut-unit partial tiles for blocks of `rows` rows (16 or 32) and of their counters.
 constexpr size_t cut_partial_bytes(int rows) {
   return static_cast<size_t>(kMaxCutUnits) * kParts * 8 * (2 * (rows / 8) * 4) * 32 * sizeof(float);

@@ -32,8 +32,8 @@
 namespace moe {
 namespace {
 
-// 32 MiB: the decode partial tiles of 16-row blocks (7.9 MB) plus the combine staging
-// of 165 tokens x top-8 x 7168 channels; every call without COMBINE fits.
+// 48 MiB: the decode partial tiles of 32-row blocks (19.9 MB) plus the combine
+// counters and rows of 263 tokens x top-8 x 7168 channels; every call without COMBINE fits.
 constexpr size_t kStaticScratchBytes = MOE_W4A16_STATIC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
