@@ -200,7 +200,6 @@ class OurArm:
             self.dom_bytes = (self.e_active * CHUNK_BYTES_PER_WEIGHT * k1 * n1 + t * k1 * 2 + r * (n1 // 2) * 2)
             self.flops = self.dom_flops + 2.0 * r * k2 * n2
             self.weight_bytes = self.e_active * CHUNK_BYTES_PER_WEIGHT * (k1 * n1 + k2 * n2)
-            self.bound = "tensor"
             self.h2d = self.a_np.nbytes + ids.nbytes + wts.nbytes
             self.d2h = t * wl.hidden * 2
         else:
@@ -244,7 +243,6 @@ class OurArm:
                               + out_rows * n * 2 + (r * n * 4 if self.flags & M.FLAG_COMBINE else 0))
             self.flops = self.dom_flops
             self.weight_bytes = self.e_active * CHUNK_BYTES_PER_WEIGHT * kd * n
-            self.bound = "hbm" if self.kernel_family == "decode" else "tensor"
             self.h2d = self.a_np.nbytes + ids.nbytes + (wts.nbytes if self.flags else 0)
             self.d2h = out_rows * n * 2
         torch.cuda.synchronize(dev)
@@ -586,7 +584,11 @@ def main(argv=None):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = e2e_ms * 1e3 / (e_steps * world)
 
-    if arm.bound == "tensor":
+    # the binding roofline: the larger of the weight/activation stream time at the HBM copy bandwidth and the
+    # contraction time at the sustained BF16 tensor rate
+    t_hbm = arm.dom_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tensor = arm.dom_flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    if t_tensor >= t_hbm:
         peak = peaks["bf16_tflops_sustained"]
         achieved = arm.dom_flops / (dom_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
@@ -599,6 +601,7 @@ def main(argv=None):
                 "traffic": None, "kernel": arm.dominant_name, "kernel_us": dom_ms * 1e3,
                 "peak_source": f"{peaks_src} hbm_gbs"}
     roof["algorithmic"] = {"flops": arm.dom_flops, "bytes": arm.dom_bytes}
+    roof["bound_us"] = {"hbm": t_hbm * 1e6, "tensor": t_tensor * 1e6}
     # DRAM bytes per launch from the committed ncu capture of this kernel and workload (null if stale or absent)
     default_wl = args.workload if not (args.tokens or args.experts or args.layout or args.block_m) else None
     roof["traffic"] = recorded_traffic(default_wl) if default_wl else None
