@@ -11,7 +11,8 @@
 //   warps 1, 3  : lane 0 issues tcgen05.mma for one 128-channel tile each
 //                 (M = 128, N = the block's rows rounded up to 16, K = 16),
 //                 A operand in TMEM, B in shared memory; one thread issues an
-//                 MMA only every ~100 cycles, so the tiles get a thread each
+//                 MMA every ~59 cycles at best (more with a commit or a branch
+//                 between MMAs), whatever N, so the tiles get a thread each
 //   warp 2      : loads the block's activation rows per k-chunk with TMA into
 //                 a 128-byte-swizzled K-major tile (16-row boxes: a block's rows
 //                 are consecutive -- indexed calls gather them in slot order first)
@@ -293,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 || warp == 3) {
     // ----------------------------------------------------- MMA issuers (warp 1: tile 0, warp 3: tile 1)
-    // A single thread issues a tcgen05.mma only every ~100 cycles, so each channel tile
-    // has its own issuing warp and accumulator; the consumers' barriers count both.
+    // One thread issues a tcgen05.mma every ~59 cycles at best whatever N, so each channel
+    // tile has its own issuing warp and accumulator; the consumers' barriers count both.
     const int mtile = warp == 1 ? 0 : 1;
     if (warp == 1) stats_base = 8;
     int xs = 0, ws = 0;
@@ -314,34 +315,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = mbar_wait(acc_empty, aph ^ 1u, abort_flag, p.err);
         ps.stop(0);
         tc_fence_after();
+        // A thread issues MMAs back to back every ~59 cycles, but each commit (~44) and each
+        // branch between them costs about as much again: no branch between the chunk's four
+        // MMAs, one test of both barriers, stage counters advanced by selects.
+        const uint32_t dacc = tmem + mtile * kAccCols;
         for (int kc = 0; ok && kc < p.KC; ++kc) {
           ps.start();
-          ok = mbar_wait(x_full + 8 * xs, xph, abort_flag, p.err);
+          const uint32_t xf = x_full + 8 * xs, wf = w_full + 8 * ws;
+          if (!(mbar_test(xf, xph) && mbar_test(wf, wph)))
+            ok = mbar_wait(xf, xph, abort_flag, p.err) && mbar_wait(wf, wph, abort_flag, p.err);
           ps.stop(1);
-          ps.start();
-          ok = ok && mbar_wait(w_full + 8 * ws, wph, abort_flag, p.err);
-          ps.stop(2);
           ps.add(3, 1);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t xa = sbase + kXOff + xs * kXBytes;
-          const uint32_t wa = tmem + kACol0 + ws * kAStageCols;   // A operand columns of this stage
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bdesc = sw128_desc(xa + ks * 32);
-            const uint32_t acc = (kc | ks) != 0;
-            tc_mma_ts(tmem + mtile * kAccCols, wa + mtile * (kAStageCols / 2) + ks * 8, bdesc, idesc, acc);
-          }
+          const uint64_t b0 = sw128_desc(sbase + kXOff + xs * kXBytes);   // + 2 per 16-k step (32 B)
+          const uint32_t wa = tmem + kACol0 + ws * kAStageCols + mtile * (kAStageCols / 2);
+          tc_mma_ts(dacc, wa, b0, idesc, kc != 0 ? 1u : 0u);
+          tc_mma_ts(dacc, wa + 8, b0 + 2, idesc, 1u);
+          tc_mma_ts(dacc, wa + 16, b0 + 4, idesc, 1u);
+          tc_mma_ts(dacc, wa + 24, b0 + 6, idesc, 1u);
           tc_commit(x_empty + 8 * xs);
           tc_commit(w_empty + 8 * ws);
-          if (++xs == kXStages) {
-            xs = 0;
-            xph ^= 1u;
-          }
-          if (++ws == kWStages) {
-            ws = 0;
-            wph ^= 1u;
-          }
+          xs = xs + 1 == kXStages ? 0 : xs + 1;
+          xph ^= xs == 0 ? 1u : 0u;
+          ws = ws + 1 == kWStages ? 0 : ws + 1;
+          wph ^= ws == 0 ? 1u : 0u;
         }
         if (ok) tc_commit(acc_full);
       }
@@ -410,7 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mj = dw >> 3;             // m-tile 2wq + mj of the tile = TMEM lanes 32wq + 16mj .. +15
     const int g = lane >> 2;
     int ps = 0, ws = 0;
-    uint32_t pph = 0, wph = 0, aph = 0;
+    uint32_t pph = 0, aph = 0;
+    uint32_t gch = 0;   // k-chunks this CTA has dequantised
     const bool swiglu = p.flags & MOE_W4A16_FLAG_SWIGLU;
     const bool combine = p.flags & MOE_W4A16_FLAG_COMBINE;
     for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
@@ -437,7 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           pph ^= 1u;
         }
         pst.start();
-        if (!warp_wait(w_empty + 8 * ws, wph ^ 1u, abort_flag, p.err)) goto d_done;
+        // the weight stage of chunk gch is free once both issuers' MMAs of chunk gch - kWStages
+        // have completed
+        if (!warp_wait(w_empty + 8 * ws, ((gch / kWStages) & 1u) ^ 1u, abort_flag, p.err)) goto d_done;
         pst.stop(1);
         pst.start();
         // A operand of this tile: TMEM lanes = channels, columns = k pairs of the 64-k chunk
@@ -464,10 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(w_full + 8 * ws);
         pst.stop(2);
-        if (++ws == kWStages) {
-          ws = 0;
-          wph ^= 1u;
-        }
+        ++gch;
+        if (++ws == kWStages) ws = 0;
       }
 
       // ------------------------------------------------- epilogue
