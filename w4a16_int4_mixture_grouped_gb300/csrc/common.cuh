@@ -318,6 +318,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 __device__ __forceinline__ float round_to_bf16(float x) { return bf16_to_f32(f32_to_bf16_rn(x)); }
 
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
+// SiLU in FP32 with the fast exponential and division intrinsics (a few ulp of FP32, far below
+// the BF16 rounding of the SwiGLU output)
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 }  // namespace moe
