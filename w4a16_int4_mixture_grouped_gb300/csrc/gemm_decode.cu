@@ -16,8 +16,10 @@
 //   * the stage is released as soon as its bytes are in registers.
 // Work units are (row block <= 32 rows, 256-channel group) in a fixed order
 // (the groups of a block, then the next block), known once the device-side
-// block count is. Each CTA's producer takes the next unit from a counter when
-// its ring has room and marks the unit's first stage for its consumers. The
+// block count is. Each CTA's producer takes the next piece (a unit, or one of
+// the k-ranges the last units of a small call are cut into) from a counter when
+// its ring has room, and writes into the piece's first stage a record with the
+// piece and its rows, from which the consumers take it. The
 // page prefers a semi-static schedule to a dynamic one (186 us vs 216 us); on
 // sm_103a with two or three CTAs per SM the warp schedulers favour the oldest
 // CTA, so CTAs given equal static shares finish far apart, while units handed
