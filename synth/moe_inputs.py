@@ -138,6 +138,12 @@ WORKLOADS: Dict[str, Workload] = {
                         "skewed routing, K=7168, N=512",
         ),
         Workload(
+            name="tp8_prefill_down_combine", num_tokens=8192, num_experts=384, top_k=8, hidden=7168,
+            intermediate=256, stage="down", routing="softmax",
+            description="the down GEMM of one 8-way tensor-parallel prefill rank with fused top-8 combine: "
+                        "8192 tokens, 384 experts, K=256, N=7168",
+        ),
+        Workload(
             name="tp8_prefill_ffn", num_tokens=8192, num_experts=384, top_k=8, hidden=7168, intermediate=256,
             stage="ffn", routing="softmax",
             description="one rank of an 8-way tensor-parallel prefill FFN: 8192 tokens, 384 experts, top-8, "

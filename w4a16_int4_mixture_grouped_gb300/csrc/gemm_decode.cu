@@ -90,6 +90,10 @@ struct Smem {
   int* prefix;
 };
 
+__device__ __forceinline__ void prefetch_l1(const void* ptr) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ void store_bf16(uint16_t* base, int64_t idx, float v) {
   base[idx] = f32_to_bf16_rn(v);
 }
@@ -265,6 +269,15 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     fence_mbar_init();
   }
   if (p.layout == MOE_W4A16_LAYOUT_MASKED && warp == 0) masked_prefix_warp(p, ROWS, s.prefix);
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED && warp == kConsumerWarps) {
+    // the first piece of this CTA is piece blockIdx.x; when that is a whole unit, its row block is
+    // blockIdx.x / NG: warm L1 with the block's routing entries while the block count loads
+    const int64_t blk0 = blockIdx.x / p.NG;
+    if (blk0 < p.sorted_cap / p.block_m) {
+      if (lane == 0) prefetch_l1(p.expert_ids + blk0);
+      if (lane < p.block_m) prefetch_l1(p.sorted_ids + blk0 * p.block_m + lane);
+    }
+  }
   __syncthreads();
 
   const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED ? p.block_m : ROWS;
@@ -279,11 +292,16 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     bool issued_any = false;
     PipeStats pps;
     const int X = split_units(total_units, p);
+    bool first = true;
     while (true) {
-      // pieces are handed out in order, one at a time, to whichever CTA asks next
-      int idx = 0;
-      if (lane == 0) idx = atomicAdd(p.grab, 1);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
+      // the first piece of CTA b is piece b; the later ones are handed out in order, one at a
+      // time, to whichever CTA asks next
+      int idx = static_cast<int>(blockIdx.x);
+      if (!first) {
+        if (lane == 0) idx = static_cast<int>(gridDim.x) + atomicAdd(p.grab, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+      }
+      first = false;
       Piece pc;
       if (!piece_of(idx, total_units, X, p.KC, pc)) break;
       const int u = pc.u;
