@@ -9,7 +9,9 @@ outputs with the oracle:
   at N=4096 and at one 8-way tensor-parallel shard's N=512: every routed
   row of four experts (hottest, median, coldest active, and the expert of
   token 0) on a sample of output channels;
-* decode down + top-8 combine, 128 tokens: 16 tokens on a channel sample;
+* down + top-8 combine at 128 tokens (decode kernel) and at 8192 tokens with
+  K = 256 (one tensor-parallel rank, tcgen05 kernel): 16 tokens on a channel
+  sample;
 * prefill FFN, 8192 tokens (indexed and contiguous layouts; and the indexed
   layout at the tensor-parallel shard's intermediate 256): the SwiGLU rows
   of every routed row of token 0's eight experts, all intermediate channels,
@@ -135,8 +137,9 @@ def test_decode_gate_up_sampled(name):
         assert_close(got, ref, f"{name} expert {e} ({flat.size} rows)")
 
 
-def test_decode_down_combine_sampled():
-    arm, wl = _arm("decode_down_combine")
+@pytest.mark.parametrize("name", ["decode_down_combine", "tp8_prefill_down_combine"])
+def test_down_combine_sampled(name):
+    arm, wl = _arm(name)
     out = arm.step()
     torch.cuda.synchronize()
     n, _ = wl.gemm_shape("w2")
@@ -151,7 +154,7 @@ def test_decode_down_combine_sampled():
             y[i * k + j] = O.gemm_rows(arm.a_np[t * k + j][None, :], _dequant_channels(wl, "w2", e, chans))[0]
     ref = O.combine(y, arm.wts_np[tokens])
     slack = combine_slack(y, arm.wts_np[tokens])
-    assert_close(_gpu_rows(out, tokens, chans), ref, "decode down+combine", slack=slack)
+    assert_close(_gpu_rows(out, tokens, chans), ref, f"{name}", slack=slack)
 
 
 @functools.lru_cache(maxsize=2)
