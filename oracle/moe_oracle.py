@@ -30,7 +30,7 @@ Layouts (the Chord page, section "Grouped SM90 kernels", Figure 3):
                 output flat [E*max_m, N] even for a 3-D input (section "grouped
                 operator entry points"); rows past masked_m[e] are ignored.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
   * accumulation: the dot product is taken in float64 (np.matmul) and rounded
     once to BF16; the GPU accumulates in FP32 in any order, which the BF16
     output tolerance covers;
