@@ -222,6 +222,11 @@ class OurArm:
             sched = M.plan(M.LAYOUT_INDEXED, t, k, e, n, kd)
             self.block_m = int(block_m or sched.block_m)
             self.kernel_family = "decode" if self.block_m <= 32 else "prefill"
+            if (not block_m and layout == "indexed" and sched.kernel == M.KERNEL_SPLIT
+                    and not self.flags & M.FLAG_COMBINE):
+                # experts above 32 rows on the tcgen05 kernel, the others on the decode kernel
+                self.kernel_family = "split"
+                self.flags |= M.FLAG_SPLIT
             lay = M.LAYOUT_MASKED if layout == "masked" else M.LAYOUT_INDEXED
             self.ws_small = M.workspace(lay, t, k, e, n, kd, self.block_m, 0, dev)
             gemm_flags = self.flags

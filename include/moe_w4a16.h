@@ -92,15 +92,20 @@ enum {
                                     as for the down projection; default: one row per token (row f / top_k) */
   MOE_W4A16_FLAG_A_SORTED = 8u,  /* indexed only: A holds one row per sorted_ids slot, [max_sorted, k]
                                     (the output of a call with MOE_W4A16_FLAG_OUT_SORTED) */
-  MOE_W4A16_FLAG_OUT_SORTED = 16u /* indexed only: output row = sorted_ids slot instead of flat id,
+  MOE_W4A16_FLAG_OUT_SORTED = 16u, /* indexed only: output row = sorted_ids slot instead of flat id,
                                     c is [max_sorted, n] (or n/2 with SWIGLU); padding slots are not written */
+  MOE_W4A16_FLAG_SPLIT = 32u      /* indexed only, block_m <= 32, not with COMBINE or A_SORTED: experts with
+                                    more than 32 routed rows run on the tcgen05 kernel (their rows gathered
+                                    in slot order, blocks of up to 192 rows), the others on the decode
+                                    kernel; the token-count rule applied per expert instead of per call */
 };
 
 /* GEMM kernel families (selected by moe_w4a16_plan or forced). */
 enum {
   MOE_W4A16_KERNEL_AUTO = 0,
   MOE_W4A16_KERNEL_DECODE = 1, /* warp-level MMA, dequantised weights as the MMA M operand, <= 32 rows/block */
-  MOE_W4A16_KERNEL_PREFILL = 2 /* tcgen05 MMA with TMEM accumulators, <= 256 rows/block */
+  MOE_W4A16_KERNEL_PREFILL = 2, /* tcgen05 MMA with TMEM accumulators, <= 256 rows/block */
+  MOE_W4A16_KERNEL_SPLIT = 3    /* indexed calls: both, split per expert (MOE_W4A16_FLAG_SPLIT, block_m 32) */
 };
 
 #define MOE_W4A16_MAGIC 0x34413457u /* "W4A4" little-endian tag */
@@ -125,7 +130,7 @@ typedef struct moe_w4a16_desc {
 
 /* Schedule chosen from the routed rows per expert (host pointer). */
 typedef struct moe_w4a16_schedule {
-  int32_t kernel;  /* MOE_W4A16_KERNEL_DECODE or _PREFILL */
+  int32_t kernel;  /* MOE_W4A16_KERNEL_DECODE, _PREFILL or (indexed) _SPLIT */
   int32_t block_m; /* rows per block the indexed align step must use */
   int32_t tok_e;   /* routed rows per expert the choice was made from */
   int32_t grid;    /* CTAs the GEMM launches (persistent, a multiple of the SM count) */
@@ -247,13 +252,19 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_gather_sorted(const uint16_t* src, int 
  * it). The environment variable MOE_W4A16_FORCE_KERNEL=decode|prefill
  * overrides the family (read on every call, part of the memo key). Indexed
  * block_m: 16 for the decode family at tok_e <= 4, 32 for the rest of the
- * decode family, 192 for the prefill family. `plan` is host. */
+ * decode family, 192 for the prefill family. Indexed calls with
+ * 8 <= tok_e < 64 (without a forced family) get MOE_W4A16_KERNEL_SPLIT with
+ * block_m 32: under skewed routing such calls mix experts of a few rows and
+ * experts of hundreds, and each family serves its own (the caller passes
+ * MOE_W4A16_FLAG_SPLIT; a call that also combines uses the decode family).
+ * `plan` is host. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_experts, int n, int k, int expected_m,
                                 moe_w4a16_schedule* plan);
 
 /* Workspace bytes for a GEMM call of the given layout and shape: 256 bytes of
- * header; for an indexed call on the prefill kernel (block_m > 32) whose A is
- * not already sorted, a bf16 [max_sorted, k] buffer into which the routed
+ * header; for an indexed call on the prefill kernel (block_m > 32, or with
+ * MOE_W4A16_FLAG_SPLIT) whose A is not already sorted, a bf16 [max_sorted, k]
+ * buffer into which the routed
  * activation rows are gathered in sorted_ids order (whole rows, once) so the
  * GEMM reads consecutive rows; for MOE_W4A16_FLAG_COMBINE an arrival counter
  * per (token, 256 output channels, slice) and a bf16 [num_tokens*top_k, n]
@@ -261,7 +272,9 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int to
  * (indexed block_m <= 32, masked), the FP32 partial tiles and counters of the
  * units it cuts into k-ranges: the last min(units, 152) units of a call with
  * at most 2048 (row block, 256-channel) units (152 units x 4 parts: 10.0 MB for
- * block_m <= 16, 19.9 MB for 32-row blocks and masked calls).
+ * block_m <= 16, 19.9 MB for 32-row blocks and masked calls); with
+ * MOE_W4A16_FLAG_SPLIT also the table of the tcgen05 kernel's blocks (int4
+ * [1 + R/192 + R/33]) and a per-expert int32 flag [num_experts].
  * block_m is ignored for the other grouped layout. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_workspace_size(int layout, int num_tokens, int top_k, int num_experts, int n,
                                                         int k, int block_m, uint32_t flags, size_t* bytes);

@@ -86,6 +86,12 @@ def test_workspace_size(lib):
     assert f(0, 64, 8, 384, 512, 7168, 1, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut16
     cap = 64 * 8 + 384 * 63                         # tcgen05 block sizes: gathered rows, no partial tiles
     assert f(0, 64, 8, 384, 512, 7168, 64, 0, ctypes.byref(out)) == 0 and out.value == 256 + cap * 7168 * 2
+    # split: + gathered rows [max_sorted, K] + the tcgen05 block table (1 + R/192 + R/33 entries) + expert flags
+    ms = 4096 + 384 * 31
+    cap = 4096 // 192 + 4096 // 33 + 1
+    table = -(-((cap + 1) * 16) // 256) * 256
+    assert f(0, 512, 8, 384, 4096, 7168, 32, 32, ctypes.byref(out)) == 0
+    assert out.value == 256 + ms * 7168 * 2 + cut32 + table + 384 * 4
     # combine: arrival counters + routed-row staging
     assert f(0, 128, 8, 384, 7168, 2048, 32, 2 | 4, ctypes.byref(out)) == 0
     counters = -(-(128 * 28 * 8 * 4) // 256) * 256
@@ -146,6 +152,15 @@ def test_gemm_host_checks_reject_before_launch(lib):
     assert _masked(lib, d, flags=8) == 1              # sorted-slot flags belong to the indexed layout
     assert _masked(lib, d, flags=4) == 1              # so does A_PER_ROW
     assert _masked(lib, d, flags=64) == 1             # unknown flag bit
+    assert _masked(lib, d, flags=32) == 1             # the per-expert split belongs to the indexed layout
+
+    def indexed(flags, block_m=32, weights=None):
+        return lib.moe_w4a16_indexed(FAKE, 8, 128, ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, 8, 2, block_m, weights,
+                                     ctypes.c_uint32(flags), FAKE, FAKE, ctypes.c_size_t(1 << 30), None)
+
+    assert indexed(32 | 2, weights=FAKE) == 1         # split with the fused combine
+    assert indexed(32 | 8) == 1                       # split with an already sorted A
+    assert indexed(32, block_m=64) == 1               # split takes the decode kernel's block sizes
     g = _desc()
     g.group_size = 64
     assert _masked(lib, g) == 2

@@ -320,16 +320,18 @@ def test_mode_mismatch_fails_before_launch():
     assert M.launch_count() == before
 
 
-@pytest.mark.parametrize("tokens,kernel,block_m", [(16, 1, 16), (128, 1, 16), (192, 1, 16), (256, 1, 32), (512, 1, 32),
-                                                   (1536, 2, 192), (8192, 2, 192)])
-def test_plan_picks_family_and_block_from_rows_per_expert(tokens, kernel, block_m):
-    """tok_e = T*top_k/E (384 experts, top-8): decode 16-row blocks up to 4 rows per expert,
-    decode 32-row blocks below 24, the tcgen05 family from 24 rows per expert on."""
+@pytest.mark.parametrize("tokens,kernel,block_m,masked_kernel",
+                         [(16, 1, 16, 1), (128, 1, 16, 1), (192, 1, 16, 1), (256, 1, 32, 1), (512, 3, 32, 1),
+                          (1536, 3, 32, 2), (3072, 2, 192, 2), (8192, 2, 192, 2)])
+def test_plan_picks_family_and_block_from_rows_per_expert(tokens, kernel, block_m, masked_kernel):
+    """tok_e = T*top_k/E (384 experts, top-8): decode 16-row blocks up to 4 rows per expert, decode 32-row blocks
+    below 8, the split per expert (indexed) from 8 to 63, the tcgen05 family from 64 on; masked calls switch
+    from the decode to the tcgen05 family at 24 rows per expert."""
     s = M.plan(M.LAYOUT_INDEXED, tokens, 8, 384, 4096, 7168)
     assert (s.kernel, s.block_m) == (kernel, block_m)
     assert s.tok_e == -(-tokens * 8 // 384)
     m = M.plan(M.LAYOUT_MASKED, tokens, 8, 384, 4096, 7168, expected_m=s.tok_e)
-    assert m.kernel == kernel
+    assert m.kernel == masked_kernel
 
 
 @pytest.mark.parametrize("e,t,k,kd,flags,regime", [(30, 100, 4, 448, 0, "all"), (100, 400, 4, 448, 0, "tail"),
@@ -359,3 +361,66 @@ def test_cut_units_match_the_oracle(e, t, k, kd, flags, regime):
         assert_close(runs[0], y, f"cut units e={e} t={t}")
     for r in runs[1:]:
         assert np.array_equal(r, runs[0])
+
+
+SPLIT_COUNTS = [1, 5, 31, 32, 33, 0, 64, 191, 192, 193, 400, 2]
+
+
+@pytest.mark.parametrize("counts", [SPLIT_COUNTS, [3, 7, 32, 0, 12], [33, 200, 385]])
+@pytest.mark.parametrize("block_m", [16, 32])
+def test_split_matches_oracle(counts, block_m):
+    """FLAG_SPLIT: experts above 32 rows on the tcgen05 kernel (blocks of up to 192 of their rows), the others on
+    the decode kernel; rows around 32 and the 192-row block edges, no hot expert, only hot experts; repeats are
+    bit-identical."""
+    rng = np.random.default_rng(800 + sum(counts) + block_m)
+    e, kd, n = len(counts), 256, 512
+    ids = ids_from_counts(rng, counts)
+    a = random_acts(rng, ids.shape[0], kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    ref = O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), n)
+    runs = [_indexed_run(a, qw, sc, ids, block_m, flags=M.FLAG_SPLIT) for _ in range(2)]
+    assert_close(runs[0], ref, f"split bm={block_m} counts={counts}")
+    assert np.array_equal(runs[0], runs[1])
+
+
+def test_split_swiglu_out_sorted_and_rows_per_routed_row():
+    """SwiGLU into sorted slots (the FFN's gate_up) and A with one row per routed row, top-4 routing."""
+    rng = np.random.default_rng(811)
+    e, t, k, kd, inter = 40, 300, 4, 192, 256
+    # skewed routing: experts 0-2 take 200 rows each, the other 37 about 16 each
+    ids = np.stack([np.concatenate([rng.permutation(3)[:2], 3 + rng.permutation(e - 3)[:2]]) for _ in range(t)])
+    ids = ids.astype(np.int32)
+    qw, sc = random_weights(rng, e, 2 * inter, kd)
+    a = random_acts(rng, t, kd)
+    pw = prepare_dev(qw, sc, M.MODE_GATE_UP, DEV)
+    f = M.FLAG_SPLIT | M.FLAG_SWIGLU | M.FLAG_OUT_SORTED
+    ws = M.workspace(M.LAYOUT_INDEXED, t, k, e, pw.n, pw.k, 32, f, DEV)
+    s_ids, e_ids, npp, _ = M.align(i32_to_dev(ids, DEV), e, 32, ws)
+    out = M.indexed(bits_to_dev(a, DEV), pw, s_ids, e_ids, npp, t, k, 32, ws, flags=f)
+    assert M.get_device_error(ws) == 0
+    h = O.swiglu(O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), 2 * inter))
+    slots = s_ids.cpu().numpy()[: int(npp.item())]
+    valid = slots < t * k
+    assert_close(dev_to_bits(out)[: slots.size][valid], h[slots[valid]], "split swiglu out_sorted")
+    # A with one row per routed row (the down projection's input, without the combine)
+    qw2, sc2 = random_weights(rng, e, 256, kd)
+    a2 = random_acts(rng, t * k, kd)
+    y2 = _indexed_run(a2, qw2, sc2, ids, 32, flags=M.FLAG_SPLIT, a_per_row=True)
+    assert_close(y2, O.indexed_gemm(a2, ids, lambda x: (qw2[x], sc2[x]), 256, a_per_routed_row=True),
+                 "split a per routed row")
+
+
+def test_split_rejects_combine_sorted_input_and_prefill_blocks():
+    rng = np.random.default_rng(812)
+    qw, sc = random_weights(rng, 3, 256, 64)
+    pw = prepare_dev(qw, sc, 1, DEV)
+    ids = i32_to_dev(np.array([[0], [1], [2], [1]], dtype=np.int32), DEV)
+    for bm, f in [(32, M.FLAG_SPLIT | M.FLAG_COMBINE | M.FLAG_A_PER_ROW), (32, M.FLAG_SPLIT | M.FLAG_A_SORTED),
+                  (64, M.FLAG_SPLIT)]:
+        with pytest.raises((M.MoeW4A16Error, ValueError)):
+            ws = M.workspace(M.LAYOUT_INDEXED, 4, 1, 3, 256, 64, bm, f & ~M.FLAG_A_SORTED, DEV)
+            s_ids, e_ids, npp, _ = M.align(ids, 3, bm, ws)
+            a_rows = s_ids.numel() if f & M.FLAG_A_SORTED else 4
+            w = torch.ones((4, 1), dtype=torch.float32, device=DEV)
+            M.indexed(torch.zeros((a_rows, 64), dtype=torch.bfloat16, device=DEV), pw, s_ids, e_ids, npp, 4, 1, bm,
+                      ws, flags=f, topk_weights=w if f & M.FLAG_COMBINE else None)

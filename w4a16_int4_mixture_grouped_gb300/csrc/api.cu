@@ -190,6 +190,8 @@ struct WsLayout {
   size_t cb_off = 0;
   int cb_segs = 0;   // contiguous: segments the merged block table holds
   size_t cut_off = 0, cut_bytes = 0, cutc_off = 0;
+  size_t split_off = 0, hot_off = 0;
+  int split_cap = 0;   // indexed split: entries of its block table
   size_t total = 0;
 };
 
@@ -202,7 +204,8 @@ static int cut_rows(int layout, int block_m) {
 }
 
 static bool gathers_activations(int layout, int block_m, uint32_t flags) {
-  return layout == MOE_W4A16_LAYOUT_INDEXED && block_m > kDecodeRows && !(flags & MOE_W4A16_FLAG_A_SORTED);
+  return layout == MOE_W4A16_LAYOUT_INDEXED && (block_m > kDecodeRows || (flags & MOE_W4A16_FLAG_SPLIT)) &&
+         !(flags & MOE_W4A16_FLAG_A_SORTED);
 }
 
 static moe_w4a16_status ws_layout(int layout, int num_tokens, int top_k, int num_experts, int n, int k, int block_m,
@@ -244,6 +247,15 @@ static moe_w4a16_status ws_layout(int layout, int num_tokens, int top_k, int num
     off += L->cut_bytes;
     L->cutc_off = off;
     off += align_up(kCutCounterBytes, 256);
+  }
+  if (layout == MOE_W4A16_LAYOUT_INDEXED && (flags & MOE_W4A16_FLAG_SPLIT)) {
+    const int64_t cap = split_table_cap(static_cast<int64_t>(num_tokens) * top_k);
+    if (cap > (int64_t(1) << 26)) return MOE_W4A16_ERR_UNSUPPORTED;
+    L->split_cap = static_cast<int>(cap);
+    L->split_off = off;
+    off += align_up(static_cast<size_t>(cap + 1) * 16, 256);
+    L->hot_off = off;
+    off += align_up(static_cast<size_t>(num_experts) * sizeof(int32_t), 256);
   }
   L->total = off;
   return MOE_W4A16_OK;
@@ -367,17 +379,24 @@ moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_e
   moe_w4a16_schedule pl;
   pl.tok_e = static_cast<int32_t>(tok_e > (1 << 30) ? (1 << 30) : tok_e);
   pl.kernel = tok_e < kDecodeMaxTokE ? MOE_W4A16_KERNEL_DECODE : MOE_W4A16_KERNEL_PREFILL;
+  // indexed calls between the regimes: the family is chosen per expert (a measured 12-21% on
+  // Zipf-skewed routing at 512 and 1536 tokens, the same within 2% under uniform routing)
+  if (layout == MOE_W4A16_LAYOUT_INDEXED && tok_e >= kSplitMinTokE && tok_e < kSplitMaxTokE)
+    pl.kernel = MOE_W4A16_KERNEL_SPLIT;
   if (forced_kernel() != 0) pl.kernel = forced_kernel();
   if (pl.kernel == MOE_W4A16_KERNEL_DECODE)
     pl.block_m = tok_e <= kDecodeSmallTokE ? kDecodeRowsSmall : kDecodeRows;
+  else if (pl.kernel == MOE_W4A16_KERNEL_SPLIT)
+    pl.block_m = kDecodeRows;
   else
     pl.block_m = kPrefillRows;
   const DeviceInfo& di = device_info(device);
-  pl.grid = pl.kernel == MOE_W4A16_KERNEL_DECODE ? 2 * di.sm_count : di.sm_count;
+  pl.grid = pl.kernel == MOE_W4A16_KERNEL_PREFILL ? di.sm_count : 2 * di.sm_count;
   if (log_enabled())
     std::fprintf(stderr, "[moe_w4a16] plan layout=%d T=%d top_k=%d E=%d n=%d k=%d tok_e=%d -> %s block_m=%d\n",
                  layout, num_tokens, top_k, num_experts, n, k, pl.tok_e,
-                 pl.kernel == MOE_W4A16_KERNEL_DECODE ? "decode" : "prefill", pl.block_m);
+                 pl.kernel == MOE_W4A16_KERNEL_DECODE ? "decode" : pl.kernel == MOE_W4A16_KERNEL_SPLIT ? "split" : "prefill",
+                 pl.block_m);
   {
     std::lock_guard<std::mutex> lock(mu);
     memo.emplace(key, pl);
@@ -432,12 +451,17 @@ static moe_w4a16_status check_gemm_common(int layout, int block_m, const moe_w4a
   if (static_cast<uint32_t>(k) != desc->k) return MOE_W4A16_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(a) & 15u) || (reinterpret_cast<uintptr_t>(c) & 15u))
     return MOE_W4A16_ERR_INVALID_ARG;
-  if (flags & ~31u) return MOE_W4A16_ERR_INVALID_ARG;
-  const uint32_t indexed_only = MOE_W4A16_FLAG_A_PER_ROW | MOE_W4A16_FLAG_A_SORTED | MOE_W4A16_FLAG_OUT_SORTED;
+  if (flags & ~63u) return MOE_W4A16_ERR_INVALID_ARG;
+  const uint32_t indexed_only = MOE_W4A16_FLAG_A_PER_ROW | MOE_W4A16_FLAG_A_SORTED | MOE_W4A16_FLAG_OUT_SORTED |
+                                MOE_W4A16_FLAG_SPLIT;
   if (layout != MOE_W4A16_LAYOUT_INDEXED && (flags & indexed_only)) return MOE_W4A16_ERR_INVALID_ARG;
   if ((flags & MOE_W4A16_FLAG_A_PER_ROW) && (flags & MOE_W4A16_FLAG_A_SORTED)) return MOE_W4A16_ERR_INVALID_ARG;
   if ((flags & MOE_W4A16_FLAG_OUT_SORTED) && (flags & MOE_W4A16_FLAG_COMBINE)) return MOE_W4A16_ERR_INVALID_ARG;
   if ((flags & MOE_W4A16_FLAG_SWIGLU) && (flags & MOE_W4A16_FLAG_COMBINE)) return MOE_W4A16_ERR_INVALID_ARG;
+  // a split call's two kernels write disjoint rows; the fused combine needs all of a token's rows in one kernel
+  if ((flags & MOE_W4A16_FLAG_SPLIT) &&
+      ((flags & (MOE_W4A16_FLAG_COMBINE | MOE_W4A16_FLAG_A_SORTED)) || block_m < 1 || block_m > kDecodeRows))
+    return MOE_W4A16_ERR_INVALID_ARG;
   if ((flags & MOE_W4A16_FLAG_SWIGLU) && desc->mode != MOE_W4A16_MODE_GATE_UP) return MOE_W4A16_ERR_MODE_MISMATCH;
   if ((flags & MOE_W4A16_FLAG_COMBINE) && desc->mode != MOE_W4A16_MODE_PLAIN) return MOE_W4A16_ERR_MODE_MISMATCH;
   if (num_tokens < 0 || top_k < 1) return MOE_W4A16_ERR_INVALID_ARG;
@@ -540,6 +564,28 @@ moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, int k, const m
   p.c_rows = p.out_sorted ? static_cast<int64_t>(ms) : r;
   const int kernel = block_m <= kDecodeRows ? MOE_W4A16_KERNEL_DECODE : MOE_W4A16_KERNEL_PREFILL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (flags & MOE_W4A16_FLAG_SPLIT) {
+    // experts above kSplitRows rows: a table of their slots in blocks of up to 192 rows, their
+    // token rows copied to those slots, the tcgen05 kernel over the table; the decode kernel
+    // takes the other experts' blocks
+    int4* table = reinterpret_cast<int4*>(static_cast<uint8_t*>(ws) + L.split_off);
+    int32_t* hot = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + L.hot_off);
+    uint16_t* g = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.gather_off);
+    MOE_CUDA_TRY(launch_split_table(sorted_ids, expert_ids, num_post_padded, p.sorted_cap, block_m, p.R,
+                                    p.num_experts, L.split_cap, table, hot, p.err, s));
+    MOE_CUDA_TRY(launch_gather_table(a, a_rows, k, sorted_ids, table, L.split_cap, p.R, p.a_div, g, p.err, s));
+    GemmParams q = p;
+    p.hot = hot;
+    moe_w4a16_status st2 = run_gemm(p, MOE_W4A16_KERNEL_DECODE, num_tokens, s);
+    if (st2 != MOE_W4A16_OK) return st2;
+    q.cblocks = table;
+    q.cb_cap = L.split_cap;
+    q.a = g;
+    q.a_rows = p.sorted_cap;
+    q.a_div = 1;
+    q.a_sorted = 1;
+    return run_gemm(q, MOE_W4A16_KERNEL_PREFILL, num_tokens, s);
+  }
   if (gathers_activations(MOE_W4A16_LAYOUT_INDEXED, block_m, flags)) {
     // the tcgen05 kernel reads consecutive rows: gather the routed rows once, whole, in sorted order
     uint16_t* g = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.gather_off);

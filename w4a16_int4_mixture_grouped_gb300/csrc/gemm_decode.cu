@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       int local;
       const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
       if (e < 0) continue;
+      if (p.hot != nullptr && p.hot[e]) continue;   // a split call's tcgen05 side takes this expert
       const RowRef rr = block_row(p, blk, e, local, rows_per_block, lane);
       const bool valid = rr.a_row >= 0;
       const unsigned vmask = __ballot_sync(0xffffffffu, valid);

@@ -15,7 +15,9 @@
 //                 between MMAs), whatever N, so the tiles get a thread each
 //   warp 2      : loads the block's activation rows per k-chunk with TMA into
 //                 a 128-byte-swizzled K-major tile (16-row boxes: a block's rows
-//                 are consecutive -- indexed calls gather them in slot order first)
+//                 are consecutive -- indexed calls gather them in slot order first;
+//                 the tcgen05 side of a split call takes the blocks of a table of
+//                 its experts' slots, the rows gathered to those slots)
 //   warps 4-19  : dequantise one 16-channel m-tile each per k-chunk in
 //                 registers and store it to TMEM as the MMA's A operand
 //                 (tcgen05.st), then run the epilogue from TMEM
@@ -195,6 +197,9 @@ __device__ __forceinline__ int block_extent(const GemmParams& p, int blk, int e,
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_tile) {
+  // a split call without experts above the decode kernel's rows: nothing to do (before any
+  // barrier or TMEM is set up)
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.cblocks != nullptr && p.cblocks[0].x <= 0) return;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED      ? p.block_m
+  const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED      ? (p.cblocks != nullptr ? kRows : p.block_m)
                              : p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS
                                  ? (p.cblocks != nullptr ? kRows : kContigSeg)
                                  : kRows;
@@ -583,7 +588,7 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
     attr_set[device] = true;
   }
   int64_t max_blocks;
-  if (p.layout == MOE_W4A16_LAYOUT_INDEXED) max_blocks = p.sorted_cap / p.block_m;
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED) max_blocks = p.cblocks != nullptr ? p.cb_cap : p.sorted_cap / p.block_m;
   else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) max_blocks = p.m_pad / kContigSeg;
   else max_blocks = static_cast<int64_t>(p.num_experts) * ((p.max_m + kRows - 1) / kRows);
   int64_t units = max_blocks * p.NG;

@@ -70,7 +70,10 @@ struct GemmParams {
   const int32_t* m_indices;
   int m_pad;
 
-  const int4* cblocks;       // contiguous on the tcgen05 kernel: merged row blocks (null: 128-row segments)
+  const int4* cblocks;       // tcgen05 kernel: table of row blocks {first row / slot, expert, rows, 0}: contiguous
+                             // merged blocks, or the indexed split's blocks of experts above kSplitRows rows
+  int cb_cap;                // indexed split: entries the table holds
+  const int32_t* hot;        // indexed split, decode kernel: experts (flag 1) the tcgen05 kernel takes
 
   // masked
   const int32_t* masked_m;
@@ -114,6 +117,12 @@ cudaError_t launch_gather_sorted(const uint16_t* src, int64_t src_rows, int K, c
 // Row blocks of a contiguous layout for the tcgen05 kernel (see layout.cu): table[0].x = count,
 // table[1 + b] = {first row, expert, rows, 0}; at most kMaxContigSegs segments (else an error).
 cudaError_t launch_contig_blocks(const int32_t* m_indices, int m_pad, int4* table, cudaStream_t stream);
+cudaError_t launch_split_table(const int32_t* sorted_ids, const int32_t* expert_ids, const int32_t* num_post_padded,
+                               int64_t sorted_cap, int block_m, int R, int E, int cap, int4* table, int32_t* hot,
+                               int* err, cudaStream_t stream);
+cudaError_t launch_gather_table(const uint16_t* src, int64_t src_rows, int K, const int32_t* sorted_ids,
+                                const int4* table, int cap, int R, int row_div, uint16_t* dst, int* err,
+                                cudaStream_t stream);
 
 // out[t, :] = bf16(sum_j w[t, j] * y[t*top_k + j, :]), j ascending, FP32 sums.
 cudaError_t launch_combine_rows(const uint16_t* y, const float* w, int T, int top_k, int N, uint16_t* out,
@@ -142,6 +151,14 @@ constexpr int kDecodeRowsSmall = 16;   // decode blocks this small run three CTA
 #endif
 constexpr int kPrefillRows = MOE_W4A16_PREFILL_ROWS;   // two 128-channel accumulators of 192 columns + weight stages fill TMEM
 constexpr int kContigSeg = 128;
+// Indexed split (MOE_W4A16_FLAG_SPLIT): experts with more than kSplitRows routed rows run on the
+// tcgen05 kernel in blocks of up to kPrefillRows rows; the plan proposes it for kSplitMinTokE <= tok_e <
+// kSplitMaxTokE.
+constexpr int kSplitRows = 32;
+constexpr int kSplitMinTokE = 8;
+constexpr int kSplitMaxTokE = 64;
+// Entries of the split's block table for R routed rows: every hot expert has more than kSplitRows rows.
+constexpr int64_t split_table_cap(int64_t R) { return R / kPrefillRows + R / (kSplitRows + 1) + 1; }
 constexpr int kMaxContigSegs = 2048;   // merged contiguous blocks: at most 2048 segments (262144 rows)
 
 }  // namespace moe

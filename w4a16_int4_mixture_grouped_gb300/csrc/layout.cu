@@ -385,6 +385,133 @@ cudaError_t launch_contiguous_layout(const int32_t* sorted_ids, const int32_t* e
   return cudaGetLastError();
 }
 
+// The split of an indexed call (align with block_m <= 32): the routed rows of each expert,
+// counted from its blocks; experts with more than kSplitRows rows are flagged for the
+// tcgen05 kernel and their slots cut into table blocks of up to kPrefillRows rows, in
+// expert order. table[0].x = block count; table[1 + b] = {first slot, expert, rows, 0}.
+// One CTA of 1024 threads (one expert per thread in the scan).
+__global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __restrict__ sorted_ids,
+                                                             const int32_t* __restrict__ expert_ids,
+                                                             const int32_t* __restrict__ npp, int64_t sorted_cap,
+                                                             int block_m, int R, int E, int cap,
+                                                             int4* __restrict__ table, int32_t* __restrict__ hot,
+                                                             int* err) {
+  __shared__ int cnt[MOE_W4A16_MAX_EXPERTS];
+  __shared__ int first[MOE_W4A16_MAX_EXPERTS];
+  __shared__ int wsum[32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int e = t; e < E; e += blockDim.x) {
+    cnt[e] = 0;
+    first[e] = 0x7fffffff;
+  }
+  __syncthreads();
+  int n = *npp;
+  if (n < 0 || n > sorted_cap) {
+    set_error(err, MOE_W4A16_ERR_BAD_INDEX);
+    n = n < 0 ? 0 : static_cast<int>(sorted_cap);
+  }
+  const int nb = n / block_m;
+  for (int b = t; b < nb; b += blockDim.x) {
+    const int e = expert_ids[b];
+    if (e < 0 || e >= E) {
+      set_error(err, MOE_W4A16_ERR_BAD_INDEX);
+      continue;
+    }
+    int v = 0;
+    for (int i = 0; i < block_m; ++i) {
+      const int id = sorted_ids[static_cast<int64_t>(b) * block_m + i];
+      v += (id >= 0 && id < R) ? 1 : 0;
+    }
+    atomicAdd(&cnt[e], v);
+    atomicMin(&first[e], b);
+  }
+  __syncthreads();
+  const int e = t;
+  const int c = e < E ? cnt[e] : 0;
+  const bool is_hot = c > kSplitRows;
+  const int nbk = is_hot ? (c + kPrefillRows - 1) / kPrefillRows : 0;
+  if (e < E) hot[e] = is_hot ? 1 : 0;
+  int incl = nbk;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += x;
+    }
+    wsum[lane] = v;
+  }
+  __syncthreads();
+  const int base = incl - nbk + (warp > 0 ? wsum[warp - 1] : 0);
+  const int slot0 = first[e < E ? e : 0] * block_m;
+  for (int j = 0; j < nbk; ++j) {
+    if (base + j >= cap) break;
+    const int rows = c - j * kPrefillRows < kPrefillRows ? c - j * kPrefillRows : kPrefillRows;
+    table[1 + base + j] = make_int4(slot0 + j * kPrefillRows, e, rows, 0);
+  }
+  if (t == 0) {
+    const int total = wsum[31];
+    if (total > cap) set_error(err, MOE_W4A16_ERR_CAPACITY);
+    table[0] = make_int4(total < cap ? total : cap, 0, 0, 0);
+  }
+}
+
+// The split's tcgen05 side reads consecutive rows: the token rows of the table's blocks,
+// copied to their sorted slots (other slots are left as they are and never read as
+// valid rows). One CTA per 8 rows of a table block, a warp per row.
+__global__ void __launch_bounds__(256) gather_table_kernel(const uint4* __restrict__ src, int64_t src_rows, int KV,
+                                                            const int32_t* __restrict__ sorted_ids,
+                                                            const int4* __restrict__ table, int cap, int R,
+                                                            int row_div, uint4* __restrict__ dst, int* err) {
+  constexpr int kParts = kPrefillRows / 8;
+  const int b = blockIdx.x / kParts;
+  const int i = (blockIdx.x % kParts) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  int nb = table[0].x;
+  nb = nb < 0 ? 0 : (nb > cap ? cap : nb);
+  if (b >= nb) return;
+  const int4 blk = table[1 + b];
+  if (i >= blk.z) return;
+  const int64_t slot = static_cast<int64_t>(blk.x) + i;
+  const int id = sorted_ids[slot];
+  if (id < 0 || id >= R || id / row_div >= src_rows) {
+    if (lane == 0) set_error(err, MOE_W4A16_ERR_BAD_INDEX);
+    return;
+  }
+  const uint4* s = src + static_cast<int64_t>(id / row_div) * KV;
+  uint4* d = dst + slot * KV;
+  for (int c = lane; c < KV; c += 32) d[c] = __ldg(s + c);
+}
+
+cudaError_t launch_gather_table(const uint16_t* src, int64_t src_rows, int K, const int32_t* sorted_ids,
+                                const int4* table, int cap, int R, int row_div, uint16_t* dst, int* err,
+                                cudaStream_t stream) {
+  const int64_t blocks = static_cast<int64_t>(cap) * (kPrefillRows / 8);
+  if (blocks < 1 || blocks > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
+  gather_table_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(src), src_rows, K / 8, sorted_ids, table, cap, R, row_div,
+      reinterpret_cast<uint4*>(dst), err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_table(const int32_t* sorted_ids, const int32_t* expert_ids, const int32_t* num_post_padded,
+                               int64_t sorted_cap, int block_m, int R, int E, int cap, int4* table, int32_t* hot,
+                               int* err, cudaStream_t stream) {
+  if (E < 1 || E > MOE_W4A16_MAX_EXPERTS || block_m < 1) return cudaErrorInvalidValue;
+  split_table_kernel<<<1, 1024, 0, stream>>>(sorted_ids, expert_ids, num_post_padded, sorted_cap, block_m, R, E, cap,
+                                             table, hot, err);
+  note_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_contig_blocks(const int32_t* m_indices, int m_pad, int4* table, cudaStream_t stream) {
   const int nseg = m_pad / kContigSeg;
   if (nseg > kMaxContigSegs) return cudaErrorInvalidValue;

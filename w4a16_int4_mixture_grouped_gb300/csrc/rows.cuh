@@ -4,7 +4,9 @@
 // A GEMM work unit is (row block, 256-channel group). A row block holds up to
 // `rows` routed rows of one expert:
 //   indexed    : block b of the align output, rows sorted_ids[b*block_m + i],
-//                valid when < R (the sentinel); A row = id / a_div; output row = id
+//                valid when < R (the sentinel); A row = id / a_div; output row = id.
+//                With a block table (the tcgen05 side of a split call) block b is
+//                {first slot, expert, rows} of the table: up to 192 slots of one expert
 //   contiguous : rows [b*rows, (b+1)*rows) of the padded activations; the
 //                block's expert is m_indices of its first row (-1: no work);
 //                padding rows (m_indices = -1) are invalid. With a merged
@@ -55,6 +57,14 @@ __device__ __forceinline__ void masked_prefix_warp(const GemmParams& p, int rows
 // Number of row blocks of the call.
 __device__ __forceinline__ int num_row_blocks(const GemmParams& p, int rows, const int* prefix) {
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED) {
+    if (p.cblocks != nullptr) {
+      const int nb = p.cblocks[0].x;
+      if (nb < 0 || nb > p.cb_cap) {
+        set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
+        return nb < 0 ? 0 : p.cb_cap;
+      }
+      return nb;
+    }
     int npp = *p.num_post_padded;
     if (npp < 0 || npp > p.sorted_cap) {
       set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
@@ -80,7 +90,7 @@ __device__ __forceinline__ int block_expert(const GemmParams& p, int blk, int ro
   local = 0;
   int e;
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED) {
-    e = p.expert_ids[blk];
+    e = p.cblocks != nullptr ? p.cblocks[1 + blk].y : p.expert_ids[blk];
   } else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) {
     e = p.cblocks != nullptr ? p.cblocks[1 + blk].y : p.m_indices[static_cast<int64_t>(blk) * rows];
     if (e < 0) return -1;
@@ -110,14 +120,25 @@ struct RowRef {
 __device__ __forceinline__ RowRef block_row(const GemmParams& p, int blk, int e, int local, int rows, int i) {
   RowRef r{-1, -1, -1};
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED) {
-    if (i >= p.block_m) return r;
-    const int id = p.sorted_ids[static_cast<int64_t>(blk) * p.block_m + i];
+    int slot;
+    if (p.cblocks != nullptr) {
+      const int4 b = p.cblocks[1 + blk];
+      if (i >= b.z) return r;
+      slot = b.x + i;
+      if (slot < 0 || slot >= p.sorted_cap) {
+        set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
+        return r;
+      }
+    } else {
+      if (i >= p.block_m) return r;
+      slot = blk * p.block_m + i;
+    }
+    const int id = p.sorted_ids[slot];
     if (id == p.R) return r;
     if (id < 0 || id > p.R) {
       set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
       return r;
     }
-    const int slot = blk * p.block_m + i;
     const int ar = p.a_sorted ? slot : id / p.a_div;
     if (ar >= p.a_rows) {
       set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);

@@ -16,9 +16,9 @@ from typing import Optional
 
 import torch
 
-from . import (FLAG_A_SORTED, FLAG_COMBINE, FLAG_OUT_SORTED, FLAG_SWIGLU, LAYOUT_CONTIGUOUS, LAYOUT_INDEXED,
-               MODE_GATE_UP, MODE_PLAIN, PreparedWeight, align, align_size, contiguous, contiguous_layout,
-               gather_rows, gather_sorted, indexed, plan, workspace)
+from . import (FLAG_A_SORTED, FLAG_COMBINE, FLAG_OUT_SORTED, FLAG_SPLIT, FLAG_SWIGLU, KERNEL_SPLIT, LAYOUT_CONTIGUOUS,
+               LAYOUT_INDEXED, MODE_GATE_UP, MODE_PLAIN, PreparedWeight, align, align_size, contiguous,
+               contiguous_layout, gather_rows, gather_sorted, indexed, plan, workspace)
 
 CONTIGUOUS_SEGMENT = 128
 DECODE_MAX_BLOCK_M = 32    # indexed calls with block_m above this run the tcgen05 kernel
@@ -46,6 +46,10 @@ class MoEFFN:
             self.block_m = int(block_m if block_m is not None else sched.block_m)
             self.f1 = FLAG_SWIGLU | FLAG_OUT_SORTED
             self.f2 = FLAG_COMBINE | FLAG_A_SORTED
+            if block_m is None and sched.kernel == KERNEL_SPLIT:
+                # gate_up split per expert (tcgen05 above 32 rows); the down GEMM with its fused
+                # combine stays on the decode kernel over the same 32-row layout
+                self.f1 |= FLAG_SPLIT
             max_sorted, _ = align_size(num_tokens, top_k, self.e, self.block_m)
             self.h = torch.empty((max_sorted, self.inter), dtype=torch.bfloat16, device=dev)
             if self.block_m > DECODE_MAX_BLOCK_M:
