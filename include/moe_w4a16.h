@@ -274,7 +274,8 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int to
  * at most 2048 (row block, 256-channel) units (152 units x 4 parts: 10.0 MB for
  * block_m <= 16, 19.9 MB for 32-row blocks and masked calls); with
  * MOE_W4A16_FLAG_SPLIT also the table of the tcgen05 kernel's blocks (int4
- * [1 + R/192 + R/33]) and a per-expert int32 flag [num_experts].
+ * [1 + R/192 + R/33]), a per-expert int32 flag [num_experts] and the decode
+ * kernel's block list (int32 [1 + max_blocks]).
  * block_m is ignored for the other grouped layout. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_workspace_size(int layout, int num_tokens, int top_k, int num_experts, int n,
                                                         int k, int block_m, uint32_t flags, size_t* bytes);

@@ -87,11 +87,13 @@ def test_workspace_size(lib):
     cap = 64 * 8 + 384 * 63                         # tcgen05 block sizes: gathered rows, no partial tiles
     assert f(0, 64, 8, 384, 512, 7168, 64, 0, ctypes.byref(out)) == 0 and out.value == 256 + cap * 7168 * 2
     # split: + gathered rows [max_sorted, K] + the tcgen05 block table (1 + R/192 + R/33 entries) + expert flags
+    # and the decode side's block list (1 + max_blocks int32)
     ms = 4096 + 384 * 31
     cap = 4096 // 192 + 4096 // 33 + 1
     table = -(-((cap + 1) * 16) // 256) * 256
+    flags_list = -(-((384 + 1 + ms // 32) * 4) // 256) * 256
     assert f(0, 512, 8, 384, 4096, 7168, 32, 32, ctypes.byref(out)) == 0
-    assert out.value == 256 + ms * 7168 * 2 + cut32 + table + 384 * 4
+    assert out.value == 256 + ms * 7168 * 2 + cut32 + table + flags_list
     # combine: arrival counters + routed-row staging
     assert f(0, 128, 8, 384, 7168, 2048, 32, 2 | 4, ctypes.byref(out)) == 0
     counters = -(-(128 * 28 * 8 * 4) // 256) * 256

@@ -254,8 +254,12 @@ static moe_w4a16_status ws_layout(int layout, int num_tokens, int top_k, int num
     L->split_cap = static_cast<int>(cap);
     L->split_off = off;
     off += align_up(static_cast<size_t>(cap + 1) * 16, 256);
+    // expert flags [E], then the decode side's block count and block list [1 + max_blocks]
+    size_t ms, mb;
+    moe_w4a16_status st = moe_w4a16_align_size(num_tokens, top_k, num_experts, block_m, &ms, &mb);
+    if (st != MOE_W4A16_OK) return st;
     L->hot_off = off;
-    off += align_up(static_cast<size_t>(num_experts) * sizeof(int32_t), 256);
+    off += align_up((static_cast<size_t>(num_experts) + 1 + mb) * sizeof(int32_t), 256);
   }
   L->total = off;
   return MOE_W4A16_OK;

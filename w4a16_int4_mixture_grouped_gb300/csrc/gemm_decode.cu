@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     fence_mbar_init();
   }
   if (p.layout == MOE_W4A16_LAYOUT_MASKED && warp == 0) masked_prefix_warp(p, ROWS, s.prefix);
-  if (p.layout == MOE_W4A16_LAYOUT_INDEXED && warp == kConsumerWarps) {
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.hot == nullptr && warp == kConsumerWarps) {
     // the first piece of this CTA is piece blockIdx.x; when that is a whole unit, its row block is
     // blockIdx.x / NG: warm L1 with the block's routing entries while the block count loads
     const int64_t blk0 = blockIdx.x / p.NG;
@@ -281,7 +281,15 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
   __syncthreads();
 
   const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED ? p.block_m : ROWS;
-  const int nblk = num_row_blocks(p, rows_per_block, s.prefix);
+  int nblk = num_row_blocks(p, rows_per_block, s.prefix);
+  // a split call: only the blocks of the list after the expert flags (hot[E] = count, then the
+  // block indices of the experts the tcgen05 kernel does not take)
+  const int32_t* cold = p.hot != nullptr ? p.hot + p.num_experts : nullptr;
+  if (cold != nullptr) {
+    const int nc = cold[0];
+    if (nc < 0 || nc > nblk) set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
+    nblk = nc < 0 ? 0 : (nc > nblk ? nblk : nc);
+  }
   const int64_t total_units = static_cast<int64_t>(nblk) * p.NG;
 
   if (warp == kConsumerWarps) {
@@ -305,11 +313,11 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       Piece pc;
       if (!piece_of(idx, total_units, X, p.KC, pc)) break;
       const int u = pc.u;
-      const int blk = u / p.NG, gp = u % p.NG;
+      const int gp = u % p.NG;
+      const int blk = cold != nullptr ? cold[1 + u / p.NG] : u / p.NG;
       int local;
       const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
       if (e < 0) continue;
-      if (p.hot != nullptr && p.hot[e]) continue;   // a split call's tcgen05 side takes this expert
       const RowRef rr = block_row(p, blk, e, local, rows_per_block, lane);
       const bool valid = rr.a_row >= 0;
       const unsigned vmask = __ballot_sync(0xffffffffu, valid);

@@ -461,6 +461,41 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
     if (total > cap) set_error(err, MOE_W4A16_ERR_CAPACITY);
     table[0] = make_int4(total < cap ? total : cap, 0, 0, 0);
   }
+  // the decode side's blocks: the other experts' blocks in block order, after the flags
+  // (hot[E] = count, hot[E + 1 + i] = block), so the decode kernel hands out no unit it skips
+  int32_t* cold = hot + E;
+  int carry = 0;
+  for (int b0 = 0; b0 < nb; b0 += blockDim.x) {
+    __syncthreads();   // wsum is reused
+    const int b = b0 + t;
+    int keep = 0;
+    if (b < nb) {
+      const int x = expert_ids[b];
+      keep = (x >= 0 && x < E && cnt[x] <= kSplitRows) ? 1 : 0;
+    }
+    int inc = keep;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      int v = wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      wsum[lane] = v;
+    }
+    __syncthreads();
+    const int pos = carry + inc - keep + (warp > 0 ? wsum[warp - 1] : 0);
+    if (keep) cold[1 + pos] = b;
+    carry += wsum[31];
+  }
+  if (t == 0) cold[0] = carry;
 }
 
 // The split's tcgen05 side reads consecutive rows: the token rows of the table's blocks,
