@@ -38,7 +38,8 @@ const DeviceInfo& device_info(int device) {
 // sm_103a the measured crossover sits lower: at K=7168, N=4096 the decode
 // family is faster at 11 rows per expert (1.49 vs 2.12 ms) and the tcgen05
 // family at 32 (2.15 vs 2.92 ms), where 32-row decode blocks start to split
-// experts and stream their weights twice.
+// experts and stream their weights twice. Indexed calls between kSplitMinTokE and
+// kSplitMaxTokE take the per-expert split instead (the same rule per expert).
 constexpr int kDecodeMaxTokE = 24;
 // Average routed rows per expert up to which decode row blocks hold 16 rows
 // (three CTAs per SM); above it 32 (fewer blocks per loaded expert).
