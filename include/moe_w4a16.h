@@ -294,7 +294,10 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_clear_device_error(void* ws, moe_w4a16_
  * Grouped GEMM entry points. Each computes, for every valid routed row r with
  * expert e, y[r, :] = A[row(r), :] . W_e^T (FP32 accumulation of BF16 products
  * of the dequantised weights), rounds to BF16 and applies the epilogue of
- * `flags`. Output tolerance against an exact reference: |err| <= 2e-2*(1+|ref|).
+ * `flags`. Output tolerance against an exact reference: |err| <= 2e-2*(1+|ref|);
+ * for COMBINE outputs plus sum_j |w[t, j]| * ulp_bf16(y[t*top_k + j]), because
+ * each routed row y is rounded to BF16 from an FP32 sum whose order differs from
+ * the reference's, so it may land one BF16 ulp away before it is weighted.
  * The kernel family follows moe_w4a16_plan (indexed: from block_m).
  * Errors: INVALID_ARG / UNSUPPORTED / MODE_MISMATCH / WORKSPACE before launch.
  * ------------------------------------------------------------------------- */
@@ -334,6 +337,8 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad
  * word, combine counters, combine staging rows, decode partial tiles) from one statically reserved
  * device array of MOE_W4A16_STATIC_SCRATCH_BYTES (48 MiB) per device.
  *   block_m    1..32 (decode kernel only), else INVALID_ARG
+ *   flags      as for moe_w4a16_indexed, except MOE_W4A16_FLAG_SPLIT (INVALID_ARG: it
+ *              would also run the tcgen05 kernel)
  *   scratch    optional host pointer; receives the device address of the array,
  *              whose first int32 is this call's device error word (read it with
  *              moe_w4a16_get_device_error). Owned by the library: never free it.
@@ -344,9 +349,12 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad
  * allocating library routine is called.
  * Set-up: the first call on a device, with that device current, resolves the
  * array's address (cudaGetSymbolAddress) and caches it; make that first call
- * before any stream capture.
- * Sharing: all calls on a device share the array. Each call clears the error
- * word and the combine counters on `stream` before its kernel; calls whose
+ * before any stream capture. The cached address is stale after a
+ * cudaDeviceReset of that device: reload the library before calling again.
+ * Sharing: all calls on a device share the array. Each call clears, on
+ * `stream` before its kernel, every counter a call may leave behind (the
+ * error word, the unit hand-out, combine and cut-unit counters), so a call
+ * after one that recorded a device error needs no recovery step. Calls whose
  * kernels overlap on the GPU race on the array (undefined results), so order
  * them on one stream or with events. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_indexed_noalloc(const uint16_t* a, int a_rows, int k, const moe_w4a16_desc* desc,

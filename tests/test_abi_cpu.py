@@ -169,7 +169,7 @@ def test_gemm_host_checks_reject_before_launch(lib):
 
 
 def test_noalloc_rejects_before_any_cuda_call(lib):
-    """The static-scratch entry point refuses calls whose scratch exceeds 48 MiB, and prefill block sizes."""
+    """The static-scratch entry point refuses calls whose scratch exceeds 48 MiB, prefill block sizes and the split."""
     d = _desc(e=4, n=1024, k=64)
 
     def call(t, k, block_m, flags, desc=d):
@@ -180,6 +180,7 @@ def test_noalloc_rejects_before_any_cuda_call(lib):
     assert call(8, 8, 64, 0) == 1                     # block_m above 32 runs the prefill kernel: refused
     assert call(8, 8, 0, 0) == 1
     assert call(8, 8, 16, 0, desc=None) == 1
+    assert call(8, 8, 32, 32) == 1                    # the per-expert split would run the tcgen05 kernel
 
 
 def test_launch_counter_starts_at_zero_without_gpu(lib):

@@ -410,6 +410,24 @@ moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_e
   return MOE_W4A16_OK;
 }
 
+}  // extern "C"
+
+namespace moe {
+// The decode kernel's cut-unit arrival counters inside a workspace of the given call shape:
+// offset and bytes (0 bytes: the call runs no decode kernel).
+moe_w4a16_status cut_counter_region(int layout, int num_tokens, int top_k, int num_experts, int n, int k,
+                                    int block_m, uint32_t flags, size_t* off, size_t* bytes) {
+  WsLayout L;
+  moe_w4a16_status st = ws_layout(layout, num_tokens, top_k, num_experts, n, k, block_m, flags, &L);
+  if (st != MOE_W4A16_OK) return st;
+  *off = L.cut_bytes ? L.cutc_off : 0;
+  *bytes = L.cut_bytes ? kCutCounterBytes : 0;
+  return MOE_W4A16_OK;
+}
+}  // namespace moe
+
+extern "C" {
+
 moe_w4a16_status moe_w4a16_workspace_size(int layout, int num_tokens, int top_k, int num_experts, int n, int k,
                                           int block_m, uint32_t flags, size_t* bytes) {
   if (bytes == nullptr) return MOE_W4A16_ERR_INVALID_ARG;

@@ -142,6 +142,9 @@ constexpr size_t cut_partial_bytes(int rows) {
   return static_cast<size_t>(kMaxCutUnits) * kParts * 8 * (2 * (rows / 8) * 4) * 32 * sizeof(float);
 }
 constexpr size_t kCutCounterBytes = static_cast<size_t>(kMaxCutUnits) * 8 * sizeof(int);
+// Offset and size of the cut-unit counters in the workspace of a call shape (size 0: none).
+moe_w4a16_status cut_counter_region(int layout, int num_tokens, int top_k, int num_experts, int n, int k,
+                                    int block_m, uint32_t flags, size_t* off, size_t* bytes);
 
 // Rows per block the kernels use for the contiguous / masked layouts.
 constexpr int kDecodeRows = 32;

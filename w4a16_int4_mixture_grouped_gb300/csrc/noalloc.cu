@@ -15,12 +15,18 @@
 // that device) and caches it. Make that first call before any stream capture.
 // No call allocates: no cudaMalloc / cudaFree, no allocating library routine.
 //
-// Sharing: every call on a device uses the same array. The error word and the
-// combine counters are cleared on the call's stream before its kernel runs;
-// the decode kernel's counters start at zero (static storage) and every call
-// leaves them at zero (a call that recorded a device error may not). Calls
-// whose kernels overlap on the GPU (other streams, other host threads without
-// ordering) race on the array and give undefined results.
+// The cached address belongs to the device's current context: after a
+// cudaDeviceReset (or an unload of this library) it is stale, and the library
+// must be reloaded before the next call.
+//
+// Sharing: every call on a device uses the same array. Each call clears, on
+// its stream and before its kernel runs, every counter a call may leave
+// behind: the workspace header (error word, unit hand-out counters), the
+// combine arrival counters and the cut-unit arrival counters. So a call that
+// recorded a device error (a wait that timed out mid-unit leaves counters
+// non-zero) needs no recovery step before the next call. Calls whose kernels
+// overlap on the GPU (other streams, other host threads without ordering)
+// race on the array and give undefined results.
 
 #include <cstdint>
 #include <mutex>
@@ -71,17 +77,26 @@ moe_w4a16_status moe_w4a16_indexed_noalloc(const uint16_t* a, int a_rows, int k,
                                            int num_tokens, int top_k, int block_m, const float* topk_weights,
                                            uint32_t flags, uint16_t* c, void** scratch, moe_w4a16_stream_t stream) {
   if (desc == nullptr || block_m < 1 || block_m > moe::kDecodeRows) return MOE_W4A16_ERR_INVALID_ARG;
+  // the decode kernel only: the per-expert split would also run the tcgen05 kernel
+  if (flags & MOE_W4A16_FLAG_SPLIT) return MOE_W4A16_ERR_INVALID_ARG;
   size_t need = 0;
   moe_w4a16_status st = moe_w4a16_workspace_size(MOE_W4A16_LAYOUT_INDEXED, num_tokens, top_k,
                                                  static_cast<int>(desc->num_experts), static_cast<int>(desc->n), k,
                                                  block_m, flags, &need);
   if (st != MOE_W4A16_OK) return st;
   if (need > moe::kStaticScratchBytes) return MOE_W4A16_ERR_SCRATCH_LIMIT;
+  size_t cut_off = 0, cut_bytes = 0;
+  st = moe::cut_counter_region(MOE_W4A16_LAYOUT_INDEXED, num_tokens, top_k, static_cast<int>(desc->num_experts),
+                               static_cast<int>(desc->n), k, block_m, flags, &cut_off, &cut_bytes);
+  if (st != MOE_W4A16_OK) return st;
   void* ws = nullptr;
   if (moe::scratch_address(&ws) != cudaSuccess) return MOE_W4A16_ERR_CUDA;
   if (scratch != nullptr) *scratch = ws;
-  // the error word reports this call; the combine counters are zeroed by the GEMM call itself
-  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  // the header (error word, hand-out counters) and the cut-unit counters start at zero whatever the
+  // previous call left; the combine counters are zeroed by the GEMM call itself
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, MOE_W4A16_WS_HEADER_BYTES, s) != cudaSuccess) return MOE_W4A16_ERR_CUDA;
+  if (cut_bytes != 0 && cudaMemsetAsync(static_cast<uint8_t*>(ws) + cut_off, 0, cut_bytes, s) != cudaSuccess)
     return MOE_W4A16_ERR_CUDA;
   return moe_w4a16_indexed(a, a_rows, k, desc, prepared, sorted_ids, expert_ids, num_post_padded, num_tokens, top_k,
                            block_m, topk_weights, flags, c, ws, moe::kStaticScratchBytes, stream);
