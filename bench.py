@@ -94,11 +94,15 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """nvidia-smi samples every 100 ms; stop() summarises those taken inside the marked windows (all of them when
+    no window was marked)."""
+
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.lines = []
         self.thread = None
+        self.windows = []
 
     def start(self):
         try:
@@ -113,9 +117,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
-    def stop(self):
+    def mark(self, t0: float, t1: float):
+        """A timed window [t0, t1] in time.perf_counter() seconds."""
+        self.windows.append((t0, t1))
+
+    def stop(self, windows=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         time.sleep(0.25)
@@ -126,9 +134,16 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
+        return self.summary(windows)
+
+    def summary(self, windows=None):
+        wins = self.windows if windows is None else windows
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in list(self.lines):
+            # a sample describes the 100 ms before it was printed
+            if wins and not any(a - 0.1 <= ts <= b + 0.1 for a, b in wins):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -153,20 +168,48 @@ def bits_to_dev(bits: np.ndarray, dev) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
 
-def upload_weights(wl, which: str, mode: int, dev):
-    """Generates every expert's logical weights (synth) straight into device memory and prepares them."""
-    import w4a16_int4_mixture_grouped_gb300 as M
+# Generated logical weights and prepared weights, shared by every workload of one process with the same
+# (seed, GEMM, shape, experts): the decode and sweep gate_up workloads use the prefill FFN's gate_up weights
+# prepared in the plain mode, the decode down workload the FFN's down weights.
+_LOGICAL = {}
+_PREPARED = {}
+
+
+def _wkey(wl, which, dev):
     n, k = wl.gemm_shape(which)
-    qw = torch.empty((wl.num_experts, n, k // 8), dtype=torch.int32, device=dev)
-    sc = torch.empty((wl.num_experts, n, k // 32), dtype=torch.bfloat16, device=dev)
-    for e in range(wl.num_experts):
-        q, s = S.expert_weights(wl, which, e)
-        qw[e].copy_(torch.from_numpy(q))
-        sc[e].copy_(torch.from_numpy(s.view(np.int16)).view(torch.bfloat16))
-    pw = M.prepare(qw, sc, mode=mode)
-    torch.cuda.synchronize(dev)
-    del qw, sc
-    return pw
+    return (wl.seed, which, n, k, wl.num_experts, str(dev))
+
+
+def logical_weights(wl, which: str, dev):
+    """Every expert's logical weights (synth), generated once per process straight into device memory."""
+    key = _wkey(wl, which, dev)
+    if key not in _LOGICAL:
+        n, k = wl.gemm_shape(which)
+        qw = torch.empty((wl.num_experts, n, k // 8), dtype=torch.int32, device=dev)
+        sc = torch.empty((wl.num_experts, n, k // 32), dtype=torch.bfloat16, device=dev)
+        for e in range(wl.num_experts):
+            q, s = S.expert_weights(wl, which, e)
+            qw[e].copy_(torch.from_numpy(q))
+            sc[e].copy_(torch.from_numpy(s.view(np.int16)).view(torch.bfloat16))
+        _LOGICAL[key] = (qw, sc)
+    return _LOGICAL[key]
+
+
+def upload_weights(wl, which: str, mode: int, dev):
+    """The prepared weights of one GEMM of a workload in one mode (cached per process)."""
+    import w4a16_int4_mixture_grouped_gb300 as M
+    key = _wkey(wl, which, dev) + (mode,)
+    if key not in _PREPARED:
+        qw, sc = logical_weights(wl, which, dev)
+        _PREPARED[key] = M.prepare(qw, sc, mode=mode)
+        torch.cuda.synchronize(dev)
+    return _PREPARED[key]
+
+
+def release_weights():
+    _LOGICAL.clear()
+    _PREPARED.clear()
+    torch.cuda.empty_cache()
 
 
 class OurArm:
@@ -357,6 +400,19 @@ class OurArm:
         comp.wait_stream(d2h)
         self.use_set(sets[0])
 
+    def e2e_serial_steps(self, host, outs, steps):
+        """`steps` steps through the API, each one in order on the current stream: the H2D copy of its
+        inputs from pinned host memory, the step, the D2H copy of its output (no overlap between steps)."""
+        a, ids, wts = host
+        for _ in range(steps):
+            self.a.copy_(a, non_blocking=True)
+            self.ids.copy_(ids, non_blocking=True)
+            if self.kind == "ffn" or self.flags:
+                self.wts.copy_(wts, non_blocking=True)
+            if needs_l2_flush(self.weight_bytes):
+                self.flush_l2()
+            outs[0].copy_(self.step(), non_blocking=True)
+
 
 # ---------------------------------------------------------------------------
 # the oracle on a bounded sample (CPU baseline and reference arm)
@@ -531,6 +587,171 @@ def config_of(wl, layout, weight_bytes=None):
             "routing": wl.routing, "seed": wl.seed, "l2": l2}
 
 
+def time_steps(arm, steps: int, stream, sampler=None):
+    """Times `steps` steps of `arm` on `stream` with CUDA events: (ms of all steps, mean µs of the dominant
+    GEMM, library launches). Workloads whose weights would fit in twice the L2 get an L2 flush before every
+    step, outside the step's own events (the steps' time is then the sum of their events)."""
+    import w4a16_int4_mixture_grouped_gb300 as M
+    dev = arm.dev
+    flush = needs_l2_flush(arm.weight_bytes)
+    dom = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    launches0 = M.launch_count()
+    w0 = time.perf_counter()
+    t0.record(stream)
+    for i in range(steps):
+        if flush:
+            arm.flush_l2()
+            step_ev[i][0].record(stream)
+        arm.step(dom[i])
+        if flush:
+            step_ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if sampler is not None:
+        sampler.mark(w0, time.perf_counter())
+    launches = M.launch_count() - launches0
+    total_ms = sum(a.elapsed_time(b) for a, b in step_ev) if flush else t0.elapsed_time(t1)
+    dom_us = float(np.mean([a.elapsed_time(b) for a, b in dom])) * 1e3
+    return total_ms, dom_us, launches
+
+
+def keep_busy(arm, seconds: float):
+    """Untimed steps for `seconds`, so the timed steps do not start on a GPU that idled."""
+    until = time.perf_counter() + seconds
+    while time.perf_counter() < until:
+        for _ in range(4):
+            arm.step()
+        torch.cuda.synchronize(arm.dev)
+
+
+def roofline_of(arm, dom_us: float, peaks, peaks_src: str):
+    """The dominant kernel against its binding roofline: the larger of its algorithmic bytes at the measured
+    HBM copy bandwidth and its flops at the measured burst BF16 rate (the kernel is timed alone per step, in a
+    run of milliseconds; the sustained rate is reported beside it)."""
+    t_hbm = arm.dom_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tensor = arm.dom_flops / (peaks["bf16_tflops"] * 1e12)
+    if t_tensor >= t_hbm:
+        achieved = arm.dom_flops / (dom_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "sustained": {"peak": peaks["bf16_tflops_sustained"],
+                              "frac": achieved / peaks["bf16_tflops_sustained"]},
+                "peak_source": f"{peaks_src} bf16_tflops (burst)"}
+    else:
+        achieved = arm.dom_bytes / (dom_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peaks_src} hbm_gbs"}
+    roof.update({"traffic": None, "kernel": arm.dominant_name, "kernel_us": dom_us,
+                 "algorithmic": {"flops": arm.dom_flops, "bytes": arm.dom_bytes},
+                 "bound_us": {"hbm": t_hbm * 1e6, "tensor": t_tensor * 1e6}})
+    return roof
+
+
+# Workloads timed beside the headline in the same run: the decode gate_up (indexed and masked), the decode
+# down + combine, one tensor-parallel rank's decode gate_up, the prefill FFN in the contiguous layout and the
+# gate_up schedule sweep.
+REGIMES = (["decode_gate_up", "decode_gate_up_masked", "decode_down_combine", "tp8_decode_gate_up",
+            "prefill_ffn_contiguous"]
+           + [f"sweep_gate_up_t{t}_{skew}" for t in S.SWEEP_TOKENS for skew in ("uniform", "zipf")])
+
+
+def host_overhead(arm, calls: int = 200):
+    """Host time to issue one GEMM call of an indexed single-GEMM workload, GPU busy behind it: through the
+    Python binding, and through the C entry point alone with pre-marshalled ctypes arguments."""
+    import ctypes
+    import w4a16_int4_mixture_grouped_gb300 as M
+    t, k = arm.wl.num_tokens, arm.wl.top_k
+    s_ids, e_ids, npp, _ = M.align(arm.ids, arm.wl.num_experts, arm.block_m, arm.ws_small, with_counts=False)
+    kwargs = dict(flags=arm.flags, topk_weights=arm.wts if arm.flags else None, out=arm.out)
+    M.indexed(arm.a, arm.w, s_ids, e_ids, npp, t, k, arm.block_m, arm.ws, **kwargs)
+    torch.cuda.synchronize(arm.dev)
+    w0 = time.perf_counter()
+    for _ in range(calls):
+        M.indexed(arm.a, arm.w, s_ids, e_ids, npp, t, k, arm.block_m, arm.ws, **kwargs)
+    binding = (time.perf_counter() - w0) / calls
+    torch.cuda.synchronize(arm.dev)
+    P = ctypes.c_void_p
+    args = (P(arm.a.data_ptr()), arm.a.shape[0], arm.a.shape[1], ctypes.byref(arm.w.desc), P(arm.w.buffer.data_ptr()),
+            P(s_ids.data_ptr()), P(e_ids.data_ptr()), P(npp.data_ptr()), t, k, arm.block_m,
+            P(arm.wts.data_ptr() if arm.flags else 0), arm.flags, P(arm.out.data_ptr()), P(arm.ws.data_ptr()),
+            arm.ws.numel(), P(torch.cuda.current_stream(arm.dev).cuda_stream))
+    fn = M.lib.moe_w4a16_indexed
+    w0 = time.perf_counter()
+    for _ in range(calls):
+        if fn(*args) != 0:
+            raise RuntimeError("moe_w4a16_indexed failed")
+    c_abi = (time.perf_counter() - w0) / calls
+    torch.cuda.synchronize(arm.dev)
+    return {"binding_us": binding * 1e6, "c_abi_us": c_abi * 1e6, "calls": calls, "workload": arm.wl.name,
+            "what": "host wall time per GEMM call (argument checks, memoised plan, launch), GPU busy behind it"}
+
+
+def measure_regimes(names, dev, steps: int, warmup: int, peaks, peaks_src, sampler):
+    out = {}
+    for name in names:
+        wl, layout = resolve(name)
+        arm = OurArm(wl, layout, dev)
+        for _ in range(warmup):
+            arm.step()
+        keep_busy(arm, 0.05)
+        total_ms, dom_us, launches = time_steps(arm, steps, torch.cuda.current_stream(dev), sampler)
+        rec = {"us_per_call": total_ms * 1e3 / steps, "steps": steps, "layout": layout, "tokens": wl.num_tokens,
+               "routing": wl.routing, "active_experts": arm.e_active, "gpu_launches": launches,
+               "l2": "flushed before every step" if needs_l2_flush(arm.weight_bytes) else "weights exceed L2"}
+        if getattr(arm, "kernel_family", None):
+            rec["kernel_family"] = arm.kernel_family
+            rec["block_m"] = arm.block_m
+        rec["roofline"] = roofline_of(arm, dom_us, peaks, peaks_src)
+        traffic = recorded_traffic(name)
+        rec["roofline"]["traffic"] = traffic
+        if name == "decode_gate_up":
+            rec["host_overhead"] = host_overhead(arm)
+        out[name] = rec
+        del arm
+        torch.cuda.empty_cache()
+    return out
+
+
+def oracle_cpu_baseline(wl, budget_s: float, single_core: bool):
+    """The oracle timed on a bounded sample of the workload, on all host cores or on one (a child process
+    pinned to one core with one BLAS thread)."""
+    if not single_core:
+        samp = OracleSample(wl)
+        v, spent, n = samp.measure(budget_s)
+        return {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                "sample": sample_text(wl, samp.channels) + f"; {n} slices, {spent:.1f} s"}
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", wl.name,
+           "--cpu-budget", str(budget_s)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=budget_s * 4 + 120)
+        rec = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.TimeoutExpired, ValueError, IndexError) as exc:
+        return {"unavailable": f"single-core oracle run failed: {exc}"}
+    return rec
+
+
+def oracle_sample_main(args):
+    """Child process of oracle_cpu_baseline(single_core=True): pins itself to one core and prints one line."""
+    try:
+        cpu = sorted(os.sched_getaffinity(0))[0]
+        os.sched_setaffinity(0, {cpu})
+    except (AttributeError, OSError):
+        pass
+    wl = resolve(args.workload)[0]
+    samp = OracleSample(wl)
+    v, spent, n = samp.measure(args.cpu_budget)
+    print(json.dumps({"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                      "sample": sample_text(wl, samp.channels) + f"; {n} slices, {spent:.1f} s, one core"}))
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -538,8 +759,10 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default="prefill_ffn")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-regimes", action="store_true", help="time only the headline workload")
+    p.add_argument("--regime-steps", type=int, default=10, help="timed steps of each workload beside the headline")
     p.add_argument("--layout", default="", choices=["", "indexed", "masked"],
                    help="override the layout of a single-GEMM workload")
     p.add_argument("--max-m", type=int, default=0, help="masked row budget per expert with --layout masked")
@@ -547,10 +770,14 @@ def main(argv=None):
                    help="indexed rows per block of a single-GEMM workload instead of the plan's (schedule sweeps)")
     p.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling cases)")
     p.add_argument("--experts", type=int, default=0, help="override the workload's expert count (profiling cases)")
+    p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     args = p.parse_args(argv)
+    if args.oracle_sample:
+        return oracle_sample_main(args)
     if args.warmup < 3:
         args.warmup = 3
     wl, layout = resolve(args.workload)
+    custom = bool(args.tokens or args.experts or args.layout or args.block_m)
     if args.tokens or args.experts:
         import dataclasses
         t = args.tokens or wl.num_tokens
@@ -569,7 +796,6 @@ def main(argv=None):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    import w4a16_int4_mixture_grouped_gb300 as M
     peaks, peaks_src = load_peaks()
     arm = OurArm(wl, layout, dev, block_m=args.block_m)
     stream = torch.cuda.current_stream(dev)
@@ -579,77 +805,44 @@ def main(argv=None):
     torch.cuda.synchronize(dev)
 
     # device-timed region: inputs resident in HBM
-    dom = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     # keep the GPU under load while the clock sampler starts, so the timed steps do not begin
     # on a GPU that idled (untimed steps, on top of the warm-up)
-    hot_until = time.perf_counter() + 0.2
-    while time.perf_counter() < hot_until:
-        for _ in range(4):
-            arm.step()
-        torch.cuda.synchronize(dev)
-    flush = needs_l2_flush(arm.weight_bytes)
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    keep_busy(arm, 0.2)
     barrier(world)
-    torch.cuda.synchronize(dev)
-    launches0 = M.launch_count()
-    t0.record(stream)
-    for i in range(args.steps):
-        if flush:
-            arm.flush_l2()
-            step_ev[i][0].record(stream)
-        arm.step(dom[i])
-        if flush:
-            step_ev[i][1].record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    launches = M.launch_count() - launches0
-    clocks = sampler.stop()
+    total_ms, dom_us, launches = time_steps(arm, args.steps, stream, sampler)
+    head_window = list(sampler.windows)
     barrier(world)
-    # with L2 flushes, the time of the steps alone (their own events), not of the flushes between them
-    total_ms = sum(a.elapsed_time(b) for a, b in step_ev) if flush else t0.elapsed_time(t1)
     total_ms = max_over_ranks(total_ms, world, dev)
-    dom_ms = float(np.mean([a.elapsed_time(b) for a, b in dom]))
     ms_per_step = total_ms / args.steps
     value = total_ms * 1e3 / (args.steps * world)
 
-    # end to end through the API with host buffers (every step's copies inside the timed region)
+    # end to end through the API with host buffers (every step's copies inside the timed region): each step
+    # serially on one stream (the per-call figure), and pipelined with the neighbouring steps' copies
     host, host_outs = arm.host_inputs()
-    arm.e2e_steps(host, host_outs, 3, dev)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_steps = max(3, min(args.steps, 20))
-    e0.record(stream)
-    arm.e2e_steps(host, host_outs, e_steps, dev)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    e2e_value = e2e_ms * 1e3 / (e_steps * world)
+    e2e = {"unit": UNIT, "h2d_bytes_per_step": int(arm.h2d), "d2h_bytes_per_step": int(arm.d2h), "steps": e_steps}
+    for mode in ("serial", "pipelined"):
+        run = (lambda n: arm.e2e_serial_steps(host, host_outs, n)) if mode == "serial" else \
+            (lambda n: arm.e2e_steps(host, host_outs, n, dev))
+        run(3)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run(e_steps)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e[mode] = e_ms * 1e3 / (e_steps * world)
+    e2e["value"] = e2e["serial"]
+    e2e["what"] = ("value: each step's H2D copies, kernels and D2H copy in order on one stream (serial); "
+                   "pipelined: H2D of step i+1 and D2H of step i-1 on two copy streams beside step i")
 
-    # the binding roofline: the larger of the weight/activation stream time at the HBM copy bandwidth and the
-    # contraction time at the sustained BF16 tensor rate
-    t_hbm = arm.dom_bytes / (peaks["hbm_gbs"] * 1e9)
-    t_tensor = arm.dom_flops / (peaks["bf16_tflops_sustained"] * 1e12)
-    if t_tensor >= t_hbm:
-        peak = peaks["bf16_tflops_sustained"]
-        achieved = arm.dom_flops / (dom_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "kernel": arm.dominant_name, "kernel_us": dom_ms * 1e3,
-                "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step)"}
-    else:
-        peak = peaks["hbm_gbs"]
-        achieved = arm.dom_bytes / (dom_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "kernel": arm.dominant_name, "kernel_us": dom_ms * 1e3,
-                "peak_source": f"{peaks_src} hbm_gbs"}
-    roof["algorithmic"] = {"flops": arm.dom_flops, "bytes": arm.dom_bytes}
-    roof["bound_us"] = {"hbm": t_hbm * 1e6, "tensor": t_tensor * 1e6}
+    roof = roofline_of(arm, dom_us, peaks, peaks_src)
     # DRAM bytes per launch from the committed ncu capture of this kernel and workload (null if stale or absent)
-    default_wl = args.workload if not (args.tokens or args.experts or args.layout or args.block_m) else None
-    roof["traffic"] = recorded_traffic(default_wl) if default_wl else None
+    roof["traffic"] = recorded_traffic(args.workload) if not custom else None
     config = config_of(wl, layout, arm.weight_bytes)
     if getattr(arm, "block_m", None) and layout == "indexed":
         config["block_m"] = arm.block_m
@@ -663,17 +856,23 @@ def main(argv=None):
                        "weight_gbs": arm.weight_bytes / (ms_per_step * 1e-3) / 1e9,
                        "active_experts": arm.e_active},
         "roofline": roof,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(arm.h2d),
-                "d2h_bytes_per_step": int(arm.d2h), "steps": e_steps,
-                "overlap": "H2D of step i+1 and D2H of step i-1 on two copy streams beside step i"},
-        "clocks": clocks,
+        "e2e": e2e,
+        "clocks": None,
         "gpu_launches": int(launches),
     }
+    del arm
+    torch.cuda.empty_cache()
+    if not args.no_regimes and not custom and args.workload == "prefill_ffn":
+        line["regimes"] = measure_regimes(REGIMES, dev, args.regime_steps, 3, peaks, peaks_src, sampler)
+    release_weights()
+    sampler.stop()
+    line["clocks"] = sampler.summary(head_window)
+    if "regimes" in line:
+        line["regimes_clocks"] = sampler.summary(sampler.windows[len(head_window):])
     if rank == 0 and not args.no_cpu_baseline:
-        samp = OracleSample(wl)
-        v, spent, n = samp.measure(args.cpu_budget)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": sample_text(wl, samp.channels) + f"; {n} slices, {spent:.1f} s"}
+        line["cpu_baseline"] = oracle_cpu_baseline(wl, args.cpu_budget, single_core=False)
+        if not custom:
+            line["cpu_baseline"]["single_core"] = oracle_cpu_baseline(wl, args.cpu_budget / 2, single_core=True)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

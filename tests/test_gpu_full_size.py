@@ -1,38 +1,43 @@
 """GPU parity at the full workload sizes, in the launch configuration the benchmark times.
 
 Each test builds the benchmark's own arm for a workload (same synthetic inputs,
-same plan, same sequence of library calls), runs one step, and compares
-outputs with the oracle:
+same plan, same sequence of library calls), runs one step and compares with
+the oracle, covering every routed row of every workload:
 
-* the 64-token, 8-expert indexed GEMM: every output element;
-* decode gate_up, 384 experts, top-8 skewed (indexed and masked layouts),
-  at N=4096 and at one 8-way tensor-parallel shard's N=512: every routed
-  row of four experts (hottest, median, coldest active, and the expert of
-  token 0) on a sample of output channels;
-* down + top-8 combine at 128 tokens (decode kernel) and at 8192 tokens with
-  K = 256 (one tensor-parallel rank, tcgen05 kernel): 16 tokens on a channel
-  sample;
-* prefill FFN, 8192 tokens (indexed and contiguous layouts; and the indexed
-  layout at the tensor-parallel shard's intermediate 256): the SwiGLU rows
-  of every routed row of token 0's eight experts, all intermediate channels,
-  then token 0's combined output on a channel sample;
-* the gate_up schedule sweep, 16..16384 tokens, uniform and Zipf skew:
-  three experts per point on a channel sample.
+* every output element: the 64-token, 8-expert GEMM; decode gate_up at 64
+  tokens over 384 experts, skewed (indexed and masked, and one 8-way
+  tensor-parallel rank's N = 512); decode down + top-8 combine at 128 tokens
+  (every token, every channel); the schedule-sweep points with 16, 128 and 512
+  tokens under uniform and Zipf routing;
+* every routed row on a channel sample holding channels of every 256-channel
+  work-unit group: the sweep points with 1536, 4096 and 16384 tokens, and the
+  prefill FFN's gate_up + SwiGLU (indexed, contiguous, the tensor-parallel
+  rank) on intermediate channels of every group;
+* every token on a channel sample of every group: the prefill FFN's down +
+  combine call (indexed, contiguous, tensor-parallel rank), made exactly as
+  the FFN step makes it, on a synthetic SwiGLU output placed by the oracle's
+  routing layout (whose GPU counterpart is checked bit-exact first); the
+  tensor-parallel rank's down + combine workload;
+* the whole FFN chain on token 0 (gate_up -> SwiGLU -> down -> combine, every
+  output channel).
 
-Weights are generated once per (shape, mode) and kept on the device across
-tests. The oracle computes only the sampled outputs, from its own
-dequantisation of the same seeded logical weights.
+The oracle references are computed per expert in a spawn process pool
+(tests/full_size_ref.py: the oracle's dequantisation tabulated over its whole
+domain, then its GEMM, SwiGLU and combine).
 """
 
-import functools
+import os
+import shutil
+import tempfile
 
 import numpy as np
 import pytest
 import torch
 
+import full_size_ref as F
 import oracle as O
 import synth as S
-from gpu_util import assert_close, combine_slack, dev_to_bits
+from gpu_util import assert_close, combine_slack, dev_to_bits, bits_to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -43,27 +48,40 @@ if torch.cuda.is_available():
 else:
     M = B = DEV = None
 
-_WEIGHTS = {}
-
-
-def _cached_upload(wl, which, mode, dev):
-    n, k = wl.gemm_shape(which)
-    key = (wl.seed, which, n, k, wl.num_experts, mode)
-    if key not in _WEIGHTS:
-        _WEIGHTS[key] = _orig_upload(wl, which, mode, dev)
-    return _WEIGHTS[key]
-
-
-_orig_upload = B.upload_weights if B is not None else None
+FULL_SWEEP = (16, 128, 512)
+SAMPLED_SWEEP = (1536, 4096, 16384)
 
 
 @pytest.fixture(scope="module", autouse=True)
-def _share_weights():
-    B.upload_weights = _cached_upload
+def _release_weights():
+    """The benchmark caches generated and prepared weights per process; free them after this module."""
     yield
-    B.upload_weights = _orig_upload
-    _WEIGHTS.clear()
-    torch.cuda.empty_cache()
+    B.release_weights()
+
+
+@pytest.fixture(scope="module")
+def pool():
+    p = F.make_pool()
+    yield p
+    p.close()
+    p.join()
+
+
+@pytest.fixture(scope="module")
+def files():
+    """Activation matrices written once as .npy files that the pool's processes map."""
+    d = tempfile.mkdtemp(prefix="moe_full_size_")
+    saved = {}
+
+    def put(key, arr):
+        if key not in saved:
+            path = os.path.join(d, f"{key}.npy")
+            np.save(path, np.ascontiguousarray(arr))
+            saved[key] = path
+        return saved[key]
+
+    yield put
+    shutil.rmtree(d, ignore_errors=True)
 
 
 def _arm(name):
@@ -71,33 +89,54 @@ def _arm(name):
     return B.OurArm(wl, layout, DEV), wl
 
 
-@functools.lru_cache(maxsize=64)
-def _weights_cpu(wl_key, which, e):
-    wl = S.get_workload(wl_key)
-    return S.expert_weights(wl, which, e)
-
-
-def _dequant_channels(wl, which, e, chans):
-    qw, sc = _weights_cpu(wl.name, which, int(e))
-    return O.dequant(O.unpack_int4(qw[chans]), sc[chans])
-
-
-def _channels(n, count, seed):
-    rng = np.random.default_rng(seed)
-    c = np.unique(np.concatenate([[0, n - 1], rng.choice(n, size=count, replace=False)]))
-    return c.astype(np.int64)
-
-
-def _rows_of(ids, e):
-    return np.nonzero(ids.reshape(-1) == e)[0]
-
-
-def _gpu_rows(out, rows, chans=None):
+def _take(out, rows, chans=None):
+    """GPU output rows (and channels), as BF16 bits on the host."""
     t = out[torch.from_numpy(np.asarray(rows, dtype=np.int64)).to(out.device)]
     if chans is not None:
-        t = t[:, torch.from_numpy(chans).to(out.device)]
+        t = t[:, torch.from_numpy(np.asarray(chans, dtype=np.int64)).to(out.device)]
     return dev_to_bits(t)
 
+
+def _assemble(results, key, rows_e, n_rows, width):
+    """Oracle rows per expert -> [n_rows, width] in flat-id order."""
+    ref = np.zeros((n_rows, width), dtype=np.uint16)
+    filled = np.zeros(n_rows, dtype=bool)
+    for e, rows in enumerate(rows_e):
+        if rows.size:
+            ref[rows] = results[e][key]
+            filled[rows] = True
+    assert filled.all()
+    return ref
+
+
+def _layout_rows(arm, route):
+    """Row of the FFN's intermediate tensor holding each flat id (sorted slot or contiguous row), from the
+    GPU's routing layout after checking it bit-exact against the oracle's."""
+    wl = arm.wl
+    used = int(route[2].item())
+    if arm.layout == "indexed":
+        s_ref, e_ref, npp_ref = O.align(arm.ids_np, wl.num_experts, arm.ffn.block_m)
+        assert used == npp_ref
+        assert np.array_equal(route[0][:used].cpu().numpy(), s_ref)
+        assert np.array_equal(route[1][: used // arm.ffn.block_m].cpu().numpy(), e_ref)
+        slot_ids = s_ref.astype(np.int64)
+    else:
+        row_ref, m_ref = O.contiguous_layout(arm.ids_np, wl.num_experts)
+        assert used == row_ref.size
+        assert np.array_equal(route[3][:used].cpu().numpy(), m_ref)
+        assert np.array_equal(route[4][:used].cpu().numpy(), row_ref)
+        assert (route[3][used:].cpu().numpy() == -1).all() and (route[4][used:].cpu().numpy() == -1).all()
+        slot_ids = row_ref.astype(np.int64)
+    where = np.full(wl.rows, -1, dtype=np.int64)
+    valid = (slot_ids >= 0) & (slot_ids < wl.rows)
+    where[slot_ids[valid]] = np.nonzero(valid)[0]
+    assert (where >= 0).all()
+    return where, used
+
+
+# ---------------------------------------------------------------------------------------------------------
+# the tiny GEMM
+# ---------------------------------------------------------------------------------------------------------
 
 def test_tiny_indexed_every_element():
     arm, wl = _arm("tiny_indexed")
@@ -108,108 +147,280 @@ def test_tiny_indexed_every_element():
     assert_close(dev_to_bits(out), ref, "tiny indexed, full output")
 
 
-def _sample_experts(counts, ids):
-    active = np.nonzero(counts)[0]
-    by_count = active[np.argsort(counts[active], kind="stable")]
-    picks = [by_count[-1], by_count[len(by_count) // 2], by_count[0], ids[0, 0]]
-    return list(dict.fromkeys(int(e) for e in picks))
+# ---------------------------------------------------------------------------------------------------------
+# gate_up weights (hidden 7168 -> 4096): decode, sweep, prefill FFN gate_up + SwiGLU
+# ---------------------------------------------------------------------------------------------------------
 
-
-@pytest.mark.parametrize("name", ["decode_gate_up", "decode_gate_up_masked", "tp8_decode_gate_up",
-                                  "tp8_decode_gate_up_masked"])
-def test_decode_gate_up_sampled(name):
+def _gate_up_outputs(name, chans):
+    """GPU gate_up output of a single-GEMM workload in flat-id order (all channels or `chans`)."""
     arm, wl = _arm(name)
     out = arm.step()
     torch.cuda.synchronize()
-    n, _ = wl.gemm_shape("w1")
-    k = wl.top_k
-    chans = _channels(n, 384, 11)
+    flat = np.arange(wl.rows)
     if arm.layout == "masked":
         masked_m, row_ids = O.masked_layout(arm.ids_np, wl.num_experts, wl.max_m)
-    for e in _sample_experts(arm.counts, arm.ids_np):
-        flat = _rows_of(arm.ids_np, e)
-        ref = O.gemm_rows(arm.a_np[flat // k], _dequant_channels(wl, "w1", e, chans))
-        if arm.layout == "masked":
-            assert masked_m[e] == flat.size and np.array_equal(row_ids[e, : flat.size], flat)
-            got = _gpu_rows(out, e * wl.max_m + np.arange(flat.size), chans)
-        else:
-            got = _gpu_rows(out, flat, chans)
-        assert_close(got, ref, f"{name} expert {e} ({flat.size} rows)")
+        rows = np.empty(wl.rows, dtype=np.int64)
+        for e in range(wl.num_experts):
+            rows[row_ids[e, : masked_m[e]]] = e * wl.max_m + np.arange(masked_m[e])
+        got = _take(out, rows, chans)
+    else:
+        got = _take(out, flat, chans)
+    res = (arm.ids_np, arm.a_np, got)
+    del arm, out
+    torch.cuda.empty_cache()
+    return res
 
 
-@pytest.mark.parametrize("name", ["decode_down_combine", "tp8_prefill_down_combine"])
-def test_down_combine_sampled(name):
-    arm, wl = _arm(name)
-    out = arm.step()
-    torch.cuda.synchronize()
-    n, _ = wl.gemm_shape("w2")
-    k = wl.top_k
-    chans = _channels(n, 512, 12)
-    tokens = np.unique(np.concatenate([[0, wl.num_tokens - 1],
-                                       np.random.default_rng(13).choice(wl.num_tokens, 14, replace=False)]))
-    y = np.zeros((tokens.size * k, chans.size), dtype=np.uint16)
-    for i, t in enumerate(tokens):
-        for j in range(k):
-            e = int(arm.ids_np[t, j])
-            y[i * k + j] = O.gemm_rows(arm.a_np[t * k + j][None, :], _dequant_channels(wl, "w2", e, chans))[0]
-    ref = O.combine(y, arm.wts_np[tokens])
-    slack = combine_slack(y, arm.wts_np[tokens])
-    assert_close(_gpu_rows(out, tokens, chans), ref, f"{name}", slack=slack)
+@pytest.fixture(scope="module")
+def gate_up_family(pool, files):
+    """One pass over the 384 experts of the shared gate_up weights: the GPU outputs of every workload that
+    uses them, and the oracle's rows for every routed row (all channels or the channel sample)."""
+    n, k = 4096, 7168
+    chans = F.group_channels(n, 256, 4, 101)                 # every 256-channel work-unit group
+    ichans = F.group_channels(n // 2, 128, 4, 102)           # intermediate channels of every gate/up group
+    gpu, cases = {}, []                                      # cases: (oracle key, ids, activations, chans, kind)
+    for name in ("decode_gate_up", "decode_gate_up_masked"):
+        ids, a, got = _gate_up_outputs(name, None)
+        gpu[name] = ("decode_gate_up", got)
+    cases.append(("decode_gate_up", ids, a, None, "gemm"))
+    for t in FULL_SWEEP + SAMPLED_SWEEP:
+        for skew in ("uniform", "zipf"):
+            name = f"sweep_gate_up_t{t}_{skew}"
+            ch = None if t in FULL_SWEEP else chans
+            ids, a, got = _gate_up_outputs(name, ch)
+            gpu[name] = (name, got)
+            cases.append((name, ids, a, ch, "gemm"))
+    for name in ("prefill_ffn", "prefill_ffn_contiguous"):
+        arm, wl = _arm(name)
+        f = arm.ffn
+        route = f.route(arm.ids)
+        h = f.gate_up(f.gate_up_input(arm.a, route), route)
+        torch.cuda.synchronize()
+        where, _ = _layout_rows(arm, route)
+        gpu[name] = ("prefill_ffn", _take(h, where, ichans))
+        ids, a = arm.ids_np, arm.a_np
+        del arm, f, route, h
+        torch.cuda.empty_cache()
+    cases.append(("prefill_ffn", ids, a, ichans, "swiglu"))
+
+    specs = []
+    per_case = [(key, F.rows_by_expert(ids, 384), ids.size, ch, kind) for key, ids, a, ch, kind in cases]
+    for e in range(384):
+        tasks = []
+        for (key, ids, a, ch, kind), (_, rows_e, _, _, _) in zip(cases, per_case):
+            if rows_e[e].size:
+                tasks.append((key, (files(key + "_a", a), rows_e[e] // ids.shape[1]), ch, kind))
+        specs.append(("decode_gate_up", "w1", e, tasks))
+    results = F.run_jobs(pool, specs)
+    refs = {}
+    for key, rows_e, n_rows, ch, kind in per_case:
+        width = n if ch is None else ch.size
+        refs[key] = _assemble(results, key, rows_e, n_rows, width)
+    return gpu, refs
 
 
-@functools.lru_cache(maxsize=2)
-def _prefill_token0_reference(base):
-    """Oracle SwiGLU rows of every routed row of token 0's experts, and token 0's combined output."""
-    wl = S.get_workload(base)
-    ids, wts = S.routing(wl)
-    a = S.activations(wl.seed, wl.num_tokens, wl.hidden)
-    k = wl.top_k
-    n2, _ = wl.gemm_shape("w2")
-    chans = _channels(n2, 1024, 14)
-    h_rows = {}
-    y2 = np.zeros((k, chans.size), dtype=np.uint16)
-    for j in range(k):
-        e = int(ids[0, j])
-        flat = _rows_of(ids, e)
-        qw, sc = _weights_cpu(wl.name, "w1", e)
-        h = O.swiglu(O.gemm_rows(a[flat // k], O.dequant_expert(qw, sc)))
-        h_rows[e] = (flat, h)
-        h0 = h[np.searchsorted(flat, j)]          # token 0's row j has flat id j
-        y2[j] = O.gemm_rows(h0[None, :], _dequant_channels(wl, "w2", e, chans))[0]
-    return h_rows, chans, O.combine(y2, wts[:1]), combine_slack(y2, wts[:1])
+@pytest.mark.parametrize("name", ["decode_gate_up", "decode_gate_up_masked"]
+                         + [f"sweep_gate_up_t{t}_{s}" for t in FULL_SWEEP for s in ("uniform", "zipf")])
+def test_gate_up_every_element(gate_up_family, name):
+    gpu, refs = gate_up_family
+    key, got = gpu[name]
+    assert got.shape[1] == 4096
+    assert_close(got, refs[key], f"{name}: every routed row, every channel")
 
 
-@pytest.mark.parametrize("name", ["prefill_ffn", "prefill_ffn_contiguous", "tp8_prefill_ffn"])
-def test_prefill_ffn_sampled(name):
+@pytest.mark.parametrize("name", [f"sweep_gate_up_t{t}_{s}" for t in SAMPLED_SWEEP for s in ("uniform", "zipf")])
+def test_gate_up_every_row_channel_sample(gate_up_family, name):
+    gpu, refs = gate_up_family
+    key, got = gpu[name]
+    assert_close(got, refs[key], f"{name}: every routed row, channels of every group")
+
+
+@pytest.mark.parametrize("name", ["prefill_ffn", "prefill_ffn_contiguous"])
+def test_prefill_ffn_swiglu_every_row(gate_up_family, name):
+    gpu, refs = gate_up_family
+    key, got = gpu[name]
+    assert_close(got, refs[key], f"{name}: SwiGLU of every routed row, intermediate channels of every group")
+
+
+# ---------------------------------------------------------------------------------------------------------
+# down weights (2048 -> 7168): decode down + combine, prefill FFN down + combine
+# ---------------------------------------------------------------------------------------------------------
+
+def _down_probe(name, chans):
+    """The FFN step's down + combine call on a synthetic SwiGLU output (every routed row's input drawn by
+    synth.down_input and placed by the oracle's layout), output channels `chans` of every token."""
     arm, wl = _arm(name)
     f = arm.ffn
     route = f.route(arm.ids)
-    h = f.gate_up(f.gate_up_input(arm.a, route), route)
-    out = f.down(h, route, arm.wts, arm.out)
+    where, _ = _layout_rows(arm, route)
+    h_flat = S.down_input(wl)
+    # as many rows as the gate_up call's output: one per sorted slot, or per contiguous-layout row
+    h_in = np.zeros((route[0].numel(), wl.intermediate), dtype=np.uint16)
+    h_in[where] = h_flat
+    out = f.down(bits_to_dev(h_in, DEV), route, arm.wts, arm.out)
     torch.cuda.synchronize()
-    # row of h holding each flat id: sorted_ids slots (indexed) or contiguous-layout rows
-    used = int(route[2].item())                  # valid slots / layout rows: num_post_padded
-    slot_ids = (route[0] if arm.layout == "indexed" else route[4])[:used].cpu().numpy().astype(np.int64)
-    where = np.full(wl.rows, -1, dtype=np.int64)
-    valid = (slot_ids >= 0) & (slot_ids < wl.rows)
-    where[slot_ids[valid]] = np.nonzero(valid)[0]
-    h_rows, chans, ref0, slack0 = _prefill_token0_reference(wl.name)
-    for e, (flat, href) in h_rows.items():
-        assert (where[flat] >= 0).all()
-        assert_close(_gpu_rows(h, where[flat]), href, f"{name} SwiGLU rows of expert {e}")
-    assert_close(_gpu_rows(out, [0], chans), ref0, f"{name} token 0 combined output", slack=slack0)
+    got = _take(out, np.arange(wl.num_tokens), chans)
+    res = (arm.ids_np, arm.wts_np, h_flat, got)
+    del arm, f, route, out
+    torch.cuda.empty_cache()
+    return res
 
 
-@pytest.mark.parametrize("skew", ["uniform", "zipf"])
-@pytest.mark.parametrize("tokens", S.SWEEP_TOKENS)
-def test_sweep_gate_up_sampled(tokens, skew):
-    arm, wl = _arm(f"sweep_gate_up_t{tokens}_{skew}")
+def _down_refs(pool, files, weights_wl, cases, n):
+    """Oracle down rows per case (key, ids, per-routed-row input, chans) in one pass over the experts."""
+    per_case = [(key, F.rows_by_expert(ids, 384), ids.size, ch) for key, ids, _, ch in cases]
+    specs = []
+    for e in range(384):
+        tasks = []
+        for (key, ids, h, ch), (_, rows_e, _, _) in zip(cases, per_case):
+            if rows_e[e].size:
+                tasks.append((key, (files(key + "_h", h), rows_e[e]), ch, "gemm"))
+        specs.append((weights_wl, "w2", e, tasks))
+    results = F.run_jobs(pool, specs)
+    return {key: _assemble(results, key, rows_e, n_rows, n if ch is None else ch.size)
+            for key, rows_e, n_rows, ch in per_case}
+
+
+@pytest.fixture(scope="module")
+def down_family(pool, files):
+    n = 7168
+    chans = F.group_channels(n, 256, 3, 201)
+    gpu, cases = {}, []
+    arm, wl = _arm("decode_down_combine")
     out = arm.step()
     torch.cuda.synchronize()
-    n, _ = wl.gemm_shape("w1")
+    gpu["decode_down_combine"] = ("decode_down_combine", dev_to_bits(out))
+    cases.append(("decode_down_combine", arm.ids_np, arm.a_np, None))
+    wts = {"decode_down_combine": arm.wts_np}
+    del arm, out
+    torch.cuda.empty_cache()
+    for name in ("prefill_ffn", "prefill_ffn_contiguous"):
+        ids, w, h, got = _down_probe(name, chans)
+        gpu[name] = ("prefill_ffn", got)
+    cases.append(("prefill_ffn", ids, h, chans))
+    wts["prefill_ffn"] = w
+    ys = _down_refs(pool, files, "decode_down_combine", cases, n)
+    refs = {key: (O.combine(y, wts[key]), combine_slack(y, wts[key])) for key, y in ys.items()}
+    return gpu, refs
+
+
+def test_decode_down_combine_every_element(down_family):
+    gpu, refs = down_family
+    key, got = gpu["decode_down_combine"]
+    ref, slack = refs[key]
+    assert got.shape == (128, 7168)
+    assert_close(got, ref, "decode down + combine: every token, every channel", slack=slack)
+
+
+@pytest.mark.parametrize("name", ["prefill_ffn", "prefill_ffn_contiguous"])
+def test_prefill_ffn_down_combine_every_token(down_family, name):
+    gpu, refs = down_family
+    key, got = gpu[name]
+    ref, slack = refs[key]
+    assert got.shape[0] == 8192
+    assert_close(got, ref, f"{name} down + combine: every token, channels of every group", slack=slack)
+
+
+# ---------------------------------------------------------------------------------------------------------
+# one 8-way tensor-parallel rank (intermediate 256)
+# ---------------------------------------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def tp8_family(pool, files):
+    gpu, cases = {}, []
+    for name in ("tp8_decode_gate_up", "tp8_decode_gate_up_masked"):
+        ids, a, got = _gate_up_outputs(name, None)
+        gpu[name] = ("tp8_decode_gate_up", got)
+    cases.append(("tp8_decode_gate_up", ids, a, None, "gemm"))
+    ichans = F.group_channels(256, 128, 16, 301)
+    arm, wl = _arm("tp8_prefill_ffn")
+    f = arm.ffn
+    route = f.route(arm.ids)
+    h = f.gate_up(f.gate_up_input(arm.a, route), route)
+    torch.cuda.synchronize()
+    where, _ = _layout_rows(arm, route)
+    gpu["tp8_prefill_ffn"] = ("tp8_prefill_ffn", _take(h, where, ichans))
+    cases.append(("tp8_prefill_ffn", arm.ids_np, arm.a_np, ichans, "swiglu"))
+    del arm, f, route, h
+    torch.cuda.empty_cache()
+    per_case = [(key, F.rows_by_expert(ids, 384), ids.size, ch) for key, ids, _, ch, _ in cases]
+    specs = []
+    for e in range(384):
+        tasks = []
+        for (key, ids, a, ch, kind), (_, rows_e, _, _) in zip(cases, per_case):
+            if rows_e[e].size:
+                tasks.append((key, (files(key + "_a", a), rows_e[e] // ids.shape[1]), ch, kind))
+        specs.append(("tp8_decode_gate_up", "w1", e, tasks))
+    results = F.run_jobs(pool, specs)
+    refs = {key: _assemble(results, key, rows_e, n_rows, 512 if ch is None else ch.size)
+            for key, rows_e, n_rows, ch in per_case}
+
+    # down (256 -> 7168): the FFN's down + combine call on a synthetic input, and the down-only workload
+    chans = F.group_channels(7168, 256, 3, 302)
+    down_cases, wts = [], {}
+    ids, w, hflat, got = _down_probe("tp8_prefill_ffn", chans)
+    gpu["tp8_prefill_ffn_down"] = ("tp8_prefill_ffn_down", got)
+    down_cases.append(("tp8_prefill_ffn_down", ids, hflat, chans))
+    wts["tp8_prefill_ffn_down"] = w
+    arm, wl = _arm("tp8_prefill_down_combine")
+    out = arm.step()
+    torch.cuda.synchronize()
+    gpu["tp8_prefill_down_combine"] = ("tp8_prefill_down_combine", _take(out, np.arange(wl.num_tokens), chans))
+    down_cases.append(("tp8_prefill_down_combine", arm.ids_np, arm.a_np, chans))
+    wts["tp8_prefill_down_combine"] = arm.wts_np
+    del arm, out
+    torch.cuda.empty_cache()
+    ys = _down_refs(pool, files, "tp8_prefill_down_combine", down_cases, 7168)
+    for key, y in ys.items():
+        refs[key] = (O.combine(y, wts[key]), combine_slack(y, wts[key]))
+    return gpu, refs
+
+
+@pytest.mark.parametrize("name", ["tp8_decode_gate_up", "tp8_decode_gate_up_masked"])
+def test_tp8_decode_gate_up_every_element(tp8_family, name):
+    gpu, refs = tp8_family
+    key, got = gpu[name]
+    assert got.shape[1] == 512
+    assert_close(got, refs[key], f"{name}: every routed row, every channel")
+
+
+def test_tp8_prefill_ffn_swiglu_every_row(tp8_family):
+    gpu, refs = tp8_family
+    key, got = gpu["tp8_prefill_ffn"]
+    assert_close(got, refs[key], "TP8 prefill FFN SwiGLU: every routed row, intermediate channels of both groups")
+
+
+@pytest.mark.parametrize("name", ["tp8_prefill_ffn_down", "tp8_prefill_down_combine"])
+def test_tp8_down_combine_every_token(tp8_family, name):
+    gpu, refs = tp8_family
+    key, got = gpu[name]
+    ref, slack = refs[key]
+    assert_close(got, ref, f"{name}: every token, channels of every group", slack=slack)
+
+
+# ---------------------------------------------------------------------------------------------------------
+# the FFN chain end to end
+# ---------------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["prefill_ffn", "prefill_ffn_contiguous", "tp8_prefill_ffn"])
+def test_prefill_ffn_chain_token0(name):
+    """gate_up -> SwiGLU -> down -> combine through the FFN step, token 0 against the oracle's own chain
+    (every SwiGLU row of token 0's experts, every output channel of token 0)."""
+    arm, wl = _arm(name)
+    f = arm.ffn
+    out = arm.step()
+    torch.cuda.synchronize()
     k = wl.top_k
-    chans = _channels(n, 256, tokens)
-    for e in _sample_experts(arm.counts, arm.ids_np)[:3]:
-        flat = _rows_of(arm.ids_np, e)
-        ref = O.gemm_rows(arm.a_np[flat // k], _dequant_channels(wl, "w1", e, chans))
-        assert_close(_gpu_rows(out, flat, chans), ref, f"sweep t={tokens} {skew} expert {e} ({flat.size} rows)")
+    ids = arm.ids_np
+    rows_e = F.rows_by_expert(ids, wl.num_experts)
+    y2 = np.zeros((k, wl.hidden), dtype=np.uint16)
+    for j in range(k):
+        e = int(ids[0, j])
+        flat = rows_e[e]
+        h = O.swiglu(O.gemm_rows(arm.a_np[flat // k], F.dequant_tabulated(*S.expert_weights(wl, "w1", e))))
+        h0 = h[np.searchsorted(flat, j)]               # token 0's row j has flat id j
+        y2[j] = O.gemm_rows(h0[None, :], F.dequant_tabulated(*S.expert_weights(wl, "w2", e)))[0]
+    ref = O.combine(y2, arm.wts_np[:1])
+    assert_close(_take(out, [0]), ref, f"{name} token 0, every channel", slack=combine_slack(y2, arm.wts_np[:1]))
+    del arm, f, out
+    torch.cuda.empty_cache()

@@ -332,6 +332,57 @@ def test_align_properties_and_bruteforce(block_m):
     assert npp == sum(-(-c // block_m) * block_m for c in counts)
 
 
+def test_contiguous_layout_structure_by_hand():
+    """Each expert's rows fill a 128-aligned segment, valid rows first in ascending flat id; padding rows
+    carry -1 in both arrays; experts with no rows take no segment. Checked against a layout built by hand
+    from per-expert row lists, and on properties (segment starts, counts) that a padding-first or a wrong
+    pad size would break."""
+    g = np.random.default_rng(11)
+    t, k, e_cnt = 70, 3, 7
+    used = np.array([0, 1, 2, 3, 5, 6])                             # expert 4 receives no rows
+    ids = np.stack([used[g.permutation(used.size)[:k]] for _ in range(t)]).astype(np.int32)
+    flat = ids.reshape(-1)
+    row_ids, m_idx = O.contiguous_layout(ids, e_cnt)
+    # by hand: segment of ceil(c/128)*128 rows per expert with rows, in expert order
+    want_rows, want_m = [], []
+    for e in range(e_cnt):
+        rows = [f for f in range(flat.size) if flat[f] == e]
+        if not rows:
+            continue
+        seg = -(-len(rows) // 128) * 128
+        want_rows += rows + [-1] * (seg - len(rows))
+        want_m += [e] * len(rows) + [-1] * (seg - len(rows))
+    assert np.array_equal(row_ids, np.asarray(want_rows, dtype=np.int32))
+    assert np.array_equal(m_idx, np.asarray(want_m, dtype=np.int32))
+    assert row_ids.size % 128 == 0
+    counts = np.bincount(flat, minlength=e_cnt)
+    for s0 in range(0, row_ids.size, 128):                          # segments start at multiples of 128
+        seg_m = m_idx[s0:s0 + 128]
+        e = seg_m[0]
+        assert e >= 0                                               # valid rows come first in a segment
+        nv = int((seg_m == e).sum())
+        assert np.all(seg_m[:nv] == e) and np.all(seg_m[nv:] == -1)
+        assert np.all(row_ids[s0:s0 + nv] >= 0) and np.all(np.diff(row_ids[s0:s0 + nv]) > 0)
+    assert np.array_equal(np.bincount(m_idx[m_idx >= 0], minlength=e_cnt), counts)
+    assert np.array_equal((row_ids < 0), (m_idx < 0))
+    assert row_ids.size == sum(-(-c // 128) * 128 for c in counts)
+
+
+def test_masked_layout_structure_by_hand():
+    """masked_m is the per-expert count; row_ids[e] lists expert e's flat ids in ascending order, then -1."""
+    ids = np.array([[2, 0], [0, 1], [2, 1], [1, 0], [3, 2]], dtype=np.int32)
+    masked_m, row_ids = O.masked_layout(ids, 5, 4)
+    assert masked_m.tolist() == [3, 3, 3, 1, 0]
+    assert row_ids.tolist() == [[1, 2, 7, -1], [3, 5, 6, -1], [0, 4, 9, -1], [8, -1, -1, -1], [-1, -1, -1, -1]]
+    g = np.random.default_rng(12)
+    ids = np.stack([g.permutation(9)[:3] for _ in range(40)]).astype(np.int32)
+    masked_m, row_ids = O.masked_layout(ids, 9, 40)
+    assert np.array_equal(masked_m, np.bincount(ids.reshape(-1), minlength=9))
+    for e in range(9):
+        assert np.array_equal(row_ids[e, :masked_m[e]], np.nonzero(ids.reshape(-1) == e)[0])
+        assert np.all(row_ids[e, masked_m[e]:] == -1)
+
+
 def test_masked_layout_overflow_raises():
     ids = np.zeros((5, 1), dtype=np.int32)
     with pytest.raises(ValueError):
