@@ -14,13 +14,17 @@
 //                 MMA every ~59 cycles at best (more with a commit or a branch
 //                 between MMAs), whatever N, so the tiles get a thread each
 //   warp 2      : loads the block's activation rows per k-chunk with TMA into
-//                 a 128-byte-swizzled K-major tile (16-row boxes: a block's rows
-//                 are consecutive -- indexed calls gather them in slot order first;
-//                 the tcgen05 side of a split call takes the blocks of a table of
-//                 its experts' slots, the rows gathered to those slots)
-//   warps 4-19  : dequantise one 16-channel m-tile each per k-chunk in
-//                 registers and store it to TMEM as the MMA's A operand
-//                 (tcgen05.st), then run the epilogue from TMEM
+//                 a 128-byte-swizzled K-major tile, one box per set bit of the
+//                 block's row count (boxes of 128, 64, 32 and 16 rows: each TMA
+//                 request costs about as much as its bytes, so a 176-row tile takes
+//                 three requests, not eleven). A block's rows are consecutive --
+//                 indexed calls gather them in slot order first; the tcgen05 side of
+//                 a split call takes the blocks of a table of its experts' slots,
+//                 the rows gathered to those slots
+//   warps 4-19  : two groups of eight that take alternate k-chunks: a warp
+//                 dequantises both 16-channel m-tiles of its TMEM lane quarter of
+//                 one tile in registers and stores them to TMEM as the MMA's A
+//                 operand (tcgen05.st); all sixteen then run the epilogue from TMEM
 //
 // Operands are "swapped" as in the page's decode design: the dequantised
 // weights are the MMA's M operand and the routed rows its N operand, so a
@@ -142,7 +146,14 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
-// One 2-D box (64 bf16 x 16 rows, 128-byte swizzle) -> 2 KB of shared memory.
+// Activation tensor maps of one call: the same [a_rows, K] bf16 tensor read in boxes of 64 k x
+// 16 << i rows (i = 0..3), 128-byte swizzle.
+constexpr int kXBoxKinds = 4;
+struct XMaps {
+  CUtensorMap box[kXBoxKinds];
+};
+
+// One 2-D box (64 bf16 x the map's rows, 128-byte swizzle) -> shared memory.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tmap, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -196,7 +207,7 @@ __device__ __forceinline__ int block_extent(const GemmParams& p, int blk, int e,
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_tile) {
+    prefill_gemm_kernel(const GemmParams p, const __grid_constant__ XMaps xmaps) {
   // a split call without experts above the decode kernel's rows: nothing to do (before any
   // barrier or TMEM is set up)
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.cblocks != nullptr && p.cblocks[0].x <= 0) return;
@@ -217,14 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(p_full + 8 * i, 1);
-      mbar_init(p_empty + 8 * i, kDequantWarps);
+      mbar_init(p_empty + 8 * i, kDequantWarps / 2);   // the chunk's dequantisation group
     }
     for (int i = 0; i < kXStages; ++i) {
       mbar_init(x_full + 8 * i, 1);
       mbar_init(x_empty + 8 * i, kIssuers);
     }
     for (int i = 0; i < kWStages; ++i) {
-      mbar_init(w_full + 8 * i, kDequantWarps);
+      mbar_init(w_full + 8 * i, kDequantWarps / 2);
       mbar_init(w_empty + 8 * i, kIssuers);
     }
     mbar_init(acc_full, kIssuers);
@@ -359,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ----------------------------------------------------- activation rows
-    // 16-row 2-D boxes of the block's consecutive rows; rows past the block up to the
-    // 16-row MMA edge are whatever follows (or the fill value), their columns are not stored.
+    // 2-D boxes of the block's consecutive rows; rows past the block up to the 16-row MMA
+    // edge are whatever follows (or the fill value), their columns are not stored.
     stats_base = 16;
     int stage = 0;
     uint32_t phase = 0;
@@ -383,8 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nr) * 128u);
         __syncwarp();
         const uint32_t xa = sbase + kXOff + stage * kXBytes;
-        for (int g16 = lane; g16 < (nr >> 4); g16 += 32)
-          tma_load_2d(xa + g16 * 2048, &tmap_tile, kc * kChunkK, row0 + 16 * g16, full);
+        // nr (a multiple of 16, at most 192) as a sum of 128-, 64-, 32- and 16-row boxes, largest
+        // first; lane i issues box i
+        if (lane < kXBoxKinds) {
+          const int kind = kXBoxKinds - 1 - lane;              // 128, 64, 32, 16 rows
+          const int rows = 16 << kind;
+          if (nr & rows) {
+            const int off = nr & ~(2 * rows - 1);              // rows of the larger boxes before it
+            tma_load_2d(xa + off * 128, &xmaps.box[kind], kc * kChunkK, row0 + off, full);
+          }
+        }
         issued = true;
         if (++stage == kXStages) {
           stage = 0;
@@ -409,9 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     PipeStats pst;
     const int dw = warp - 4;            // 0..15
     const int wq = dw & 3;              // TMEM lane quarter (warp % 4, the lanes this warp may access)
-    const int tile = (dw >> 2) & 1;     // channel tile (chunk) of the unit
-    const int mj = dw >> 3;             // m-tile 2wq + mj of the tile = TMEM lanes 32wq + 16mj .. +15
+    // epilogue share: accumulator column chunks tile + 2 mj, + 4, ... of lane quarter wq
+    const int tile = (dw >> 2) & 1;
+    const int mj = dw >> 3;
     const int g = lane >> 2;
+    const int grp = dw >> 3;            // dequantisation group: even (0) or odd (1) k-chunks
+    const int dq_tile = (dw >> 2) & 1;  // tile whose lane quarter wq this warp dequantises
     int ps = 0, ws = 0;
     uint32_t pph = 0, aph = 0;
     uint32_t gch = 0;   // k-chunks this CTA has dequantised
@@ -427,13 +449,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ext == 0) continue;
       const int nr = (ext + 15) & ~15;
       for (int kc = 0; kc < p.KC; ++kc) {
+        // k-chunks alternate between the two groups of eight warps (half the barrier traffic of
+        // sixteen warps per chunk, and twice the independent work per warp); the other group's
+        // chunks only advance this warp's stage counters
+        if ((gch & 1u) != static_cast<uint32_t>(grp)) {
+          if (++ps == kPStages) {
+            ps = 0;
+            pph ^= 1u;
+          }
+          ++gch;
+          if (++ws == kWStages) ws = 0;
+          continue;
+        }
         pst.start();
         if (!warp_wait(p_full + 8 * ps, pph, abort_flag, p.err)) goto d_done;
         pst.stop(0);
-        const uint32_t pa = sbase + kPOff + ps * kPBytes + tile * kChunkBytes;
-        const int mt = 2 * wq + mj;
-        const uint4 wv = lds128(pa + (mt * 32 + lane) * 16);
-        const uint2 sv = lds64(pa + kChunkWBytes + (mt * 8 + g) * 8);
+        const uint32_t pa = sbase + kPOff + ps * kPBytes + dq_tile * kChunkBytes;
+        uint4 wv[2];
+        uint2 sv[2];
+#pragma unroll
+        for (int m2 = 0; m2 < 2; ++m2) {
+          const int mt = 2 * wq + m2;
+          wv[m2] = lds128(pa + (mt * 32 + lane) * 16);
+          sv[m2] = lds64(pa + kChunkWBytes + (mt * 8 + g) * 8);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(p_empty + 8 * ps);
         if (++ps == kPStages) {
@@ -446,13 +485,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(w_empty + 8 * ws, ((gch / kWStages) & 1u) ^ 1u, abort_flag, p.err)) goto d_done;
         pst.stop(1);
         pst.start();
-        // A operand of this tile: TMEM lanes = channels, columns = k pairs of the 64-k chunk
-        const uint32_t at = tmem + kACol0 + ws * kAStageCols + tile * (kAStageCols / 2);
-        {
-          const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+        // A operand of this tile: TMEM lanes = channels (this warp's quarter), columns = k pairs of
+        // the 64-k chunk; m-tile m2 at lanes 32 wq + 16 m2
+        const uint32_t at = tmem + kACol0 + ws * kAStageCols + dq_tile * (kAStageCols / 2) +
+                            (static_cast<uint32_t>(32 * wq) << 16);
+#pragma unroll
+        for (int m2 = 0; m2 < 2; ++m2) {
+          const uint32_t w4[4] = {wv[m2].x, wv[m2].y, wv[m2].z, wv[m2].w};
           uint32_t sg[2], sg8[2];
-          scale_pairs(sv, 0, sg[0], sg8[0]);
-          scale_pairs(sv, 1, sg[1], sg8[1]);
+          scale_pairs(sv[m2], 0, sg[0], sg8[0]);
+          scale_pairs(sv[m2], 1, sg[1], sg8[1]);
           uint32_t frag[16];
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
@@ -463,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             frag[4 * ks + 2] = a[2];
             frag[4 * ks + 3] = a[3];
           }
-          tmem_st_16x128b_x8(at + (static_cast<uint32_t>(32 * wq + 16 * mj) << 16), frag);
+          tmem_st_16x128b_x8(at + (static_cast<uint32_t>(16 * m2) << 16), frag);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -565,18 +607,20 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
   using namespace prefill;
   // a block's rows must be consecutive in A (indexed calls gather them in slot order first)
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED && !p.a_sorted) return cudaErrorInvalidValue;
-  // activations as a 2-D tensor [a_rows, K] of bf16, read in 16-row x 128-byte boxes
+  // activations as a 2-D tensor [a_rows, K] of bf16, read in boxes of 128 bytes x 16, 32, 64 or 128 rows
   EncodeTiledFn enc = encode_tiled();
   if (enc == nullptr || p.a_rows < 1) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.a_rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K) * 2};
   const cuuint32_t estr[2] = {1, 1};
-  CUtensorMap tmap_tile;
-  const cuuint32_t box16[2] = {static_cast<cuuint32_t>(kChunkK), 16};
-  if (enc(&tmap_tile, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.a), dims, strides, box16, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  XMaps xmaps;
+  for (int i = 0; i < kXBoxKinds; ++i) {
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkK), static_cast<cuuint32_t>(16 << i)};
+    if (enc(&xmaps.box[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.a), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   const DeviceInfo& di = device_info(device);
   const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
   const int smem = smem_bytes(prefix_entries);
@@ -595,7 +639,7 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
   int64_t grid = di.sm_count;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  prefill_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p, tmap_tile);
+  prefill_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p, xmaps);
   note_launch();
   if (grid_out) *grid_out = static_cast<int>(grid);
   return cudaGetLastError();
