@@ -26,8 +26,8 @@
  *     row id or count is skipped and recorded in the workspace error word
  *     (read it with moe_w4a16_get_device_error); a kernel never reads or
  *     writes outside the buffers it was given, and every wait inside a
- *     kernel gives up after about two seconds and records
- *     MOE_W4A16_ERR_DEVICE_TIMEOUT instead of hanging.
+ *     kernel gives up after about two seconds (moe_w4a16_set_wait_limit_ns)
+ *     and records MOE_W4A16_ERR_DEVICE_TIMEOUT instead of hanging.
  *   - `ws` is a caller-owned workspace of at least moe_w4a16_workspace_size()
  *     bytes (always >= 256: its first bytes hold the device error word and the
  *     decode kernel's unit hand-out counters). Zero it once after allocation
@@ -113,6 +113,7 @@ enum {
 #define MOE_W4A16_MAX_EXPERTS 1024
 #define MOE_W4A16_WS_HEADER_BYTES 256
 #define MOE_W4A16_STATIC_SCRATCH_BYTES (48u << 20) /* scratch of moe_w4a16_indexed_noalloc */
+#define MOE_W4A16_WAIT_LIMIT_NS 2000000000ull      /* default limit of a device pipeline wait */
 
 /* Host-side description of a prepared weight, filled by moe_w4a16_prepare and
  * passed by address to every GEMM call (host pointer). */
@@ -286,6 +287,19 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_workspace_init(void* ws, size_t ws_byte
 /* Synchronises `stream`, then copies the device error word of `ws` to *code
  * (host): MOE_W4A16_OK or the first device-detected error since the last clear. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_get_device_error(const void* ws, moe_w4a16_stream_t stream, int32_t* code);
+
+/* Diagnostics and tests: sets, for the current device, the limit after which a
+ * GEMM kernel's pipeline wait gives up (default MOE_W4A16_WAIT_LIMIT_NS, about
+ * two seconds; larger values are INVALID_ARG). A wait that runs out records
+ * MOE_W4A16_ERR_DEVICE_TIMEOUT in the workspace error word; the kernel then
+ * stops its CTA's pipeline, lets copies already in flight land (those drains
+ * keep the default limit), releases its tensor memory and returns. Below 20 us
+ * the waits poll without suspending, so with a limit of 0 the first wait for
+ * data that has not arrived yet gives up at once. Applies to the GEMM calls
+ * made after it on that device, from any thread, until set again. Recover from
+ * the error with moe_w4a16_workspace_init on the workspace (counters may be
+ * left non-zero). */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_set_wait_limit_ns(uint64_t ns);
 
 /* Resets the device error word (async on stream). */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_clear_device_error(void* ws, moe_w4a16_stream_t stream);

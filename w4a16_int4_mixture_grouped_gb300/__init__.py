@@ -76,6 +76,7 @@ _SIGNATURES = {
     "moe_w4a16_workspace_init": (_I, [_P, _SZ, _P]),
     "moe_w4a16_get_device_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_w4a16_clear_device_error": (_I, [_P, _P]),
+    "moe_w4a16_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "moe_w4a16_indexed": (_I, [_P, _I, _I, ctypes.POINTER(Desc), _P, _P, _P, _P, _I, _I, _I, _P, _U32, _P, _P, _SZ,
                                _P]),
     "moe_w4a16_contiguous": (_I, [_P, _I, _I, _P, ctypes.POINTER(Desc), _P, _P, _I, _I, _P, _U32, _P, _P, _SZ, _P]),
@@ -255,6 +256,17 @@ def get_device_error(ws: torch.Tensor) -> int:
         _check(_lib.moe_w4a16_get_device_error(_ptr(ws), _stream(ws.device), ctypes.byref(code)),
                "get_device_error")
     return int(code.value)
+
+
+WAIT_LIMIT_NS = 2_000_000_000   # default limit of a device pipeline wait
+
+
+def set_wait_limit_ns(ns: int, device=None) -> None:
+    """Diagnostics and tests: the limit after which a GEMM kernel's pipeline wait gives up, on `device`
+    (default WAIT_LIMIT_NS; 0 makes the first wait for data not yet arrived give up at once)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        _check(_lib.moe_w4a16_set_wait_limit_ns(int(ns)), "set_wait_limit_ns")
 
 
 def clear_device_error(ws: torch.Tensor) -> None:

@@ -16,6 +16,16 @@
 namespace moe {
 
 static std::atomic<uint64_t> g_launches{0};
+
+// Wait limit of the GEMM launches per device (moe_w4a16_set_wait_limit_ns).
+constexpr int kMaxWaitDevices = 64;
+static std::atomic<uint64_t> g_wait_ns[kMaxWaitDevices] = {};
+static std::atomic<bool> g_wait_set{false};
+uint64_t wait_limit_ns(int device) {
+  if (!g_wait_set.load(std::memory_order_relaxed) || device < 0 || device >= kMaxWaitDevices)
+    return MOE_W4A16_WAIT_LIMIT_NS;
+  return g_wait_ns[device].load(std::memory_order_relaxed);
+}
 void note_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
 const DeviceInfo& device_info(int device) {
@@ -453,6 +463,18 @@ moe_w4a16_status moe_w4a16_get_device_error(const void* ws, moe_w4a16_stream_t s
   return MOE_W4A16_OK;
 }
 
+moe_w4a16_status moe_w4a16_set_wait_limit_ns(uint64_t ns) {
+  if (ns > MOE_W4A16_WAIT_LIMIT_NS) return MOE_W4A16_ERR_INVALID_ARG;
+  int device = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&device));
+  if (device < 0 || device >= kMaxWaitDevices) return MOE_W4A16_ERR_INVALID_ARG;
+  if (!g_wait_set.exchange(true)) {
+    for (int d = 0; d < kMaxWaitDevices; ++d) g_wait_ns[d].store(MOE_W4A16_WAIT_LIMIT_NS, std::memory_order_relaxed);
+  }
+  g_wait_ns[device].store(ns, std::memory_order_relaxed);
+  return MOE_W4A16_OK;
+}
+
 moe_w4a16_status moe_w4a16_clear_device_error(void* ws, moe_w4a16_stream_t stream) {
   if (ws == nullptr) return MOE_W4A16_ERR_INVALID_ARG;
   MOE_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)));
@@ -534,6 +556,7 @@ static void fill_common(GemmParams& p, const moe_w4a16_desc* desc, const void* p
 static moe_w4a16_status run_gemm(GemmParams& p, int kernel, int num_tokens, cudaStream_t stream) {
   int device = 0;
   MOE_CUDA_TRY(cudaGetDevice(&device));
+  p.wait_ns = wait_limit_ns(device);
   const bool combine = p.flags & MOE_W4A16_FLAG_COMBINE;
   if (combine) p.c_rows = num_tokens;
   int grid = 0;

@@ -57,9 +57,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Upper bound of any single pipeline wait. A wait that runs out records
-// MOE_W4A16_ERR_DEVICE_TIMEOUT, raises the CTA's abort flag and returns false.
+// Upper bound of any single pipeline wait, unless the host lowered it for a launch
+// (GemmParams::wait_ns; diagnostics and tests through moe_w4a16_set_wait_limit_ns). A wait
+// that runs out records MOE_W4A16_ERR_DEVICE_TIMEOUT, raises the CTA's abort flag and returns
+// false. The drains of copies still in flight after an abort always use kWaitLimitNs.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Longest time a waiting thread asks to be suspended for at once; a limit below it makes the
+// waits poll without suspending (and skip the potentially blocking first test), so that the
+// limit is what ends them.
+constexpr uint32_t kSuspendNs = 20000u;
 
 // try_wait that may suspend the thread for up to `hint_ns` while the phase is incomplete.
 __device__ __forceinline__ bool mbar_test_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
@@ -74,14 +80,33 @@ __device__ __forceinline__ bool mbar_test_suspend(uint32_t bar, uint32_t parity,
   return ok != 0;
 }
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_now(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, bool suspend) {
+  return suspend ? mbar_test_suspend(bar, parity, kSuspendNs) : mbar_test_now(bar, parity);
+}
+
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                                   uint64_t limit) {
   const uint64_t t0 = global_timer_ns();
+  const bool suspend = limit >= kSuspendNs;
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (mbar_test_suspend(bar, parity, 20000u)) return true;
+      if (mbar_poll(bar, parity, suspend)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 >= limit) {
       set_error(err, MOE_W4A16_ERR_DEVICE_TIMEOUT);
       if (abort_flag != nullptr) *abort_flag = 1;
       return false;
@@ -89,25 +114,27 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  if (mbar_test(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, err);
+// Bounded wait for the phase with the given parity to complete (limit: the launch's wait_ns).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          uint64_t limit) {
+  if (limit >= kSuspendNs && mbar_test(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, limit);
 }
 
 static __device__ __noinline__ bool warp_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                   int* err) {
+                                                   int* err, uint64_t limit) {
   const bool leader = (threadIdx.x & 31) == 0;
   const uint64_t t0 = global_timer_ns();
+  const bool suspend = limit >= kSuspendNs;
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (__all_sync(0xffffffffu, mbar_test_suspend(bar, parity, 20000u))) return true;
+      if (__all_sync(0xffffffffu, mbar_poll(bar, parity, suspend))) return true;
     int stop = 0;
     if (leader) {
       if (abort_flag != nullptr && *abort_flag) {
         stop = 1;
-      } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+      } else if (global_timer_ns() - t0 >= limit) {
         set_error(err, MOE_W4A16_ERR_DEVICE_TIMEOUT);
         if (abort_flag != nullptr) *abort_flag = 1;
         stop = 1;
@@ -122,9 +149,10 @@ static __device__ __noinline__ bool warp_wait_slow(uint32_t bar, uint32_t parity
 // give-up decision is lane 0's, broadcast, so a timeout never splits a warp in
 // front of a warp-collective operation. A completed phase cannot move on
 // under a lane, because the next phase needs this warp's own release.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
-  return warp_wait_slow(bar, parity, abort_flag, err);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          uint64_t limit) {
+  if (limit >= kSuspendNs && __all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  return warp_wait_slow(bar, parity, abort_flag, err, limit);
 }
 
 // Warp-uniform read of the CTA's abort flag.

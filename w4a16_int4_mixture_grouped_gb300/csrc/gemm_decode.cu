@@ -115,7 +115,7 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
   const uint32_t act_lane = 2 * kChunkBytes + (lane & 7) * kActStride + (lane >> 3) * 16;
   for (int kc = 0; kc < nkc; ++kc) {
     ps.start();
-    if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) return false;
+    if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err, p.wait_ns)) return false;
     ps.stop(0);
     ps.add(1, 1);
     const uint32_t sb = s.stages + stage * Geo<ROWS>::kStageBytes;
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       const int kc0 = pc.kc0, kc1 = pc.kc1;
       for (int kc = kc0; kc < kc1; ++kc) {
         pps.start();
-        if (!warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err)) goto producer_done;
+        if (!warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err, p.wait_ns)) goto producer_done;
         pps.stop(0);
         pps.add(1, 1);
         const uint32_t full = s.full + 8 * stage;
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       }
     }
     // no more units: one stage carries the end mark (33 plain arrivals complete its phase)
-    if (warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err)) {
+    if (warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err, p.wait_ns)) {
       if (lane == 0) {
         recs[stage * kRecInts + kRecIdx] = -1;
         mbar_arrive(s.full + 8 * stage);
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     while (true) {
       cps.stop(3);   // epilogue of the previous unit (and unit bookkeeping)
       // the next piece is the one the producer put at the head of the current stage
-      if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err)) goto consumer_done;
+      if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err, p.wait_ns)) goto consumer_done;
       const int* rec = recs + stage * kRecInts;
       if (rec[kRecIdx] < 0) break;
       const int gp = rec[kRecGroup], ntiles = rec[kRecTiles];

@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ok = 1;
         if (lane == 0) {
           ps.start();
-          ok = mbar_wait(p_empty + 8 * stage, phase ^ 1u, abort_flag, p.err);
+          ok = mbar_wait(p_empty + 8 * stage, phase ^ 1u, abort_flag, p.err, p.wait_ns);
           ps.stop(0);
           if (ok) {
             const uint32_t full = p_full + 8 * stage;
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16(128, nr);
       if (lane == 0) {
         ps.start();
-        bool ok = mbar_wait(acc_empty, aph ^ 1u, abort_flag, p.err);
+        bool ok = mbar_wait(acc_empty, aph ^ 1u, abort_flag, p.err, p.wait_ns);
         ps.stop(0);
         tc_fence_after();
         // A thread issues MMAs back to back every ~59 cycles, but each commit (~44) and each
@@ -338,8 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kc = 0; ok && kc < p.KC; ++kc) {
           ps.start();
           const uint32_t xf = x_full + 8 * xs, wf = w_full + 8 * ws;
-          if (!(mbar_test(xf, xph) && mbar_test(wf, wph)))
-            ok = mbar_wait(xf, xph, abort_flag, p.err) && mbar_wait(wf, wph, abort_flag, p.err);
+          if (!(p.wait_ns >= kSuspendNs && mbar_test(xf, xph) && mbar_test(wf, wph)))
+            ok = mbar_wait(xf, xph, abort_flag, p.err, p.wait_ns) && mbar_wait(wf, wph, abort_flag, p.err, p.wait_ns);
           ps.stop(1);
           ps.add(3, 1);
           if (!ok) break;
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = block_row(p, blk, e, local, rows_per_block, 0).a_row;
       for (int kc = 0; kc < p.KC; ++kc) {
         ps.start();
-        if (!warp_wait(x_empty + 8 * stage, phase ^ 1u, abort_flag, p.err)) goto x_done;
+        if (!warp_wait(x_empty + 8 * stage, phase ^ 1u, abort_flag, p.err, p.wait_ns)) goto x_done;
         ps.stop(0);
         const uint32_t full = x_full + 8 * stage;
         if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nr) * 128u);
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         pst.start();
-        if (!warp_wait(p_full + 8 * ps, pph, abort_flag, p.err)) goto d_done;
+        if (!warp_wait(p_full + 8 * ps, pph, abort_flag, p.err, p.wait_ns)) goto d_done;
         pst.stop(0);
         const uint32_t pa = sbase + kPOff + ps * kPBytes + dq_tile * kChunkBytes;
         uint4 wv[2];
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pst.start();
         // the weight stage of chunk gch is free once both issuers' MMAs of chunk gch - kWStages
         // have completed
-        if (!warp_wait(w_empty + 8 * ws, ((gch / kWStages) & 1u) ^ 1u, abort_flag, p.err)) goto d_done;
+        if (!warp_wait(w_empty + 8 * ws, ((gch / kWStages) & 1u) ^ 1u, abort_flag, p.err, p.wait_ns)) goto d_done;
         pst.stop(1);
         pst.start();
         // A operand of this tile: TMEM lanes = channels (this warp's quarter), columns = k pairs of
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ------------------------------------------------- epilogue
       pst.start();
-      if (!warp_wait(acc_full, aph, abort_flag, p.err)) goto d_done;
+      if (!warp_wait(acc_full, aph, abort_flag, p.err, p.wait_ns)) goto d_done;
       pst.stop(3);
       pst.start();
       aph ^= 1u;

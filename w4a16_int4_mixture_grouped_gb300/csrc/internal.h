@@ -95,7 +95,11 @@ struct GemmParams {
   int64_t c_rows;            // rows of c (bounds)
   int c_cols;                // row length of c (N, or N/2 with SWIGLU)
   int* err;                  // device error word
+  uint64_t wait_ns;          // limit of a pipeline wait (moe_w4a16_set_wait_limit_ns)
 };
+
+// The wait limit of launches on `device` (MOE_W4A16_WAIT_LIMIT_NS unless lowered).
+uint64_t wait_limit_ns(int device);
 
 cudaError_t launch_prepare(const int32_t* qweight, const uint16_t* scales, int E, int N, int K, int mode,
                            uint8_t* prepared, cudaStream_t stream);
