@@ -215,7 +215,7 @@ def release_weights():
 class OurArm:
     """Holds device inputs and runs one step of the hot path for a workload."""
 
-    def __init__(self, wl, layout: str, dev, block_m: int = 0):
+    def __init__(self, wl, layout: str, dev, block_m: int = 0, routed: bool = True):
         import w4a16_int4_mixture_grouped_gb300 as M
         from w4a16_int4_mixture_grouped_gb300.pipeline import MoEFFN
         self.M, self.wl, self.layout, self.dev = M, wl, layout, dev
@@ -279,6 +279,9 @@ class OurArm:
                 max_sorted, _ = M.align_size(t, k, e, self.block_m)
                 self.a_sorted = torch.empty((max_sorted, kd), dtype=torch.bfloat16, device=dev)
             self.ws = M.workspace(lay, t, k, e, n, kd, self.block_m, gemm_flags, dev)
+            # decode-family indexed calls take the router's ids straight: one launch per call (each CTA
+            # builds the block layout itself) instead of align + GEMM
+            self.routed = (routed and layout == "indexed" and self.kernel_family == "decode" and r <= M.ROUTED_MAX_ROWS)
             if layout == "masked":
                 self.max_m = wl.max_m
                 self.expected_m = max(1, int(self.counts[self.counts > 0].mean())) if self.e_active else 1
@@ -307,6 +310,14 @@ class OurArm:
             if ev:
                 ev[0].record()
             M.masked(self.a3, mm, self.expected_m, self.w, self.ws, flags=self.flags, out=self.out)
+            if ev:
+                ev[1].record()
+            return self.out
+        if self.routed:
+            if ev:
+                ev[0].record()
+            M.indexed_routed(self.a, self.w, self.ids, self.block_m, self.ws, flags=self.flags,
+                             topk_weights=self.wts if self.flags else None, out=self.out)
             if ev:
                 ev[1].record()
             return self.out
@@ -685,8 +696,16 @@ def host_overhead(arm, calls: int = 200):
             raise RuntimeError("moe_w4a16_indexed failed")
     c_abi = (time.perf_counter() - w0) / calls
     torch.cuda.synchronize(arm.dev)
-    return {"binding_us": binding * 1e6, "c_abi_us": c_abi * 1e6, "calls": calls, "workload": arm.wl.name,
-            "what": "host wall time per GEMM call (argument checks, memoised plan, launch), GPU busy behind it"}
+    w0 = time.perf_counter()
+    for _ in range(calls):
+        M.indexed_routed(arm.a, arm.w, arm.ids, arm.block_m, arm.ws, **kwargs)
+    routed = (time.perf_counter() - w0) / calls
+    torch.cuda.synchronize(arm.dev)
+    return {"binding_us": binding * 1e6, "c_abi_us": c_abi * 1e6, "routed_binding_us": routed * 1e6, "calls": calls,
+            "workload": arm.wl.name,
+            "what": "host wall time per GEMM call (argument checks, memoised plan, launch), GPU busy behind it: "
+                    "indexed GEMM through the binding and through the C entry point alone, and the one-launch "
+                    "routed GEMM through the binding"}
 
 
 def measure_regimes(names, dev, steps: int, warmup: int, peaks, peaks_src, sampler):
@@ -702,7 +721,7 @@ def measure_regimes(names, dev, steps: int, warmup: int, peaks, peaks_src, sampl
                "routing": wl.routing, "active_experts": arm.e_active, "gpu_launches": launches,
                "l2": "flushed before every step" if needs_l2_flush(arm.weight_bytes) else "weights exceed L2"}
         if getattr(arm, "kernel_family", None):
-            rec["kernel_family"] = arm.kernel_family
+            rec["kernel_family"] = arm.kernel_family + (" (routed, one launch)" if getattr(arm, "routed", False) else "")
             rec["block_m"] = arm.block_m
         rec["roofline"] = roofline_of(arm, dom_us, peaks, peaks_src)
         traffic = recorded_traffic(name)
@@ -768,6 +787,8 @@ def main(argv=None):
     p.add_argument("--max-m", type=int, default=0, help="masked row budget per expert with --layout masked")
     p.add_argument("--block-m", type=int, default=0,
                    help="indexed rows per block of a single-GEMM workload instead of the plan's (schedule sweeps)")
+    p.add_argument("--no-routed", action="store_true",
+                   help="decode-family indexed workloads: align + GEMM instead of the one-launch routed GEMM")
     p.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling cases)")
     p.add_argument("--experts", type=int, default=0, help="override the workload's expert count (profiling cases)")
     p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
@@ -797,7 +818,7 @@ def main(argv=None):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks, peaks_src = load_peaks()
-    arm = OurArm(wl, layout, dev, block_m=args.block_m)
+    arm = OurArm(wl, layout, dev, block_m=args.block_m, routed=not args.no_routed)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
@@ -846,7 +867,7 @@ def main(argv=None):
     config = config_of(wl, layout, arm.weight_bytes)
     if getattr(arm, "block_m", None) and layout == "indexed":
         config["block_m"] = arm.block_m
-        config["kernel"] = arm.kernel_family
+        config["kernel"] = arm.kernel_family + (" (routed, one launch)" if getattr(arm, "routed", False) else "")
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -114,6 +114,7 @@ enum {
 #define MOE_W4A16_WS_HEADER_BYTES 256
 #define MOE_W4A16_STATIC_SCRATCH_BYTES (48u << 20) /* scratch of moe_w4a16_indexed_noalloc */
 #define MOE_W4A16_WAIT_LIMIT_NS 2000000000ull      /* default limit of a device pipeline wait */
+#define MOE_W4A16_ROUTED_MAX_ROWS 4096             /* routed rows of a moe_w4a16_indexed_routed call */
 
 /* Host-side description of a prepared weight, filled by moe_w4a16_prepare and
  * passed by address to every GEMM call (host pointer). */
@@ -328,6 +329,30 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, 
                                    const int32_t* num_post_padded, int num_tokens, int top_k, int block_m,
                                    const float* topk_weights, uint32_t flags, uint16_t* c, void* ws, size_t ws_bytes,
                                    moe_w4a16_stream_t stream);
+
+/* Indexed layout straight from the router's output, in one launch (the Chord
+ * page, sections "H200 and Blackwell indexed decode": the token-tile schedule is
+ * resolved mostly up front and refined by the actual token counts, and "Grouped
+ * SM90 kernels": repeated host-side resolution is what memoisation removes).
+ * Every CTA of the decode kernel builds, in its own shared memory, the block
+ * layout that moe_w4a16_align would build (experts in ascending order, each
+ * expert's routed rows in ascending flat id, blocks of block_m rows), so the
+ * call needs neither an align launch nor sorted_ids / expert_ids arrays. The
+ * result is the one of moe_w4a16_align + moe_w4a16_indexed with the same
+ * block_m, bit for bit.
+ *   topk_ids   int32 [T, top_k], expert ids in [0, E); an id outside is skipped and
+ *              recorded as MOE_W4A16_ERR_BAD_INDEX in `ws`
+ *   block_m    1..32 (the decode kernel), else INVALID_ARG
+ *   flags      as for moe_w4a16_indexed except A_SORTED, OUT_SORTED and SPLIT (INVALID_ARG)
+ *   T*top_k    at most MOE_W4A16_ROUTED_MAX_ROWS (4096), else UNSUPPORTED
+ *   ws         at least moe_w4a16_workspace_size(MOE_W4A16_LAYOUT_INDEXED, ..., block_m, flags)
+ * Other arguments and outputs as for moe_w4a16_indexed. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_indexed_routed(const uint16_t* a, int a_rows, int k,
+                                                        const moe_w4a16_desc* desc, const void* prepared,
+                                                        const int32_t* topk_ids, int num_tokens, int top_k,
+                                                        int block_m, const float* topk_weights, uint32_t flags,
+                                                        uint16_t* c, void* ws, size_t ws_bytes,
+                                                        moe_w4a16_stream_t stream);
 
 /* Contiguous layout (the Chord page, Figure 3: each expert padded to a 128-row
  * boundary; valid rows of a segment come first).

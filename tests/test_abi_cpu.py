@@ -186,3 +186,26 @@ def test_noalloc_rejects_before_any_cuda_call(lib):
 def test_launch_counter_starts_at_zero_without_gpu(lib):
     lib.moe_w4a16_launch_count.restype = ctypes.c_uint64
     assert lib.moe_w4a16_launch_count() == 0
+
+
+def test_routed_rejects_before_any_cuda_call(lib):
+    """The one-launch routed entry point refuses prefill block sizes, the sorted-slot and split flags, more
+    routed rows than a CTA's routing table holds, and a missing id array."""
+    d = _desc(e=4, n=256, k=128)
+    fn = lib.moe_w4a16_indexed_routed
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+
+    def call(t, k, block_m, flags=0, ids=FAKE, a_rows=None):
+        return fn(FAKE, t if a_rows is None else a_rows, 128, ctypes.byref(d), FAKE, ids, t, k, block_m, None,
+                  ctypes.c_uint32(flags), FAKE, FAKE, ctypes.c_size_t(1 << 30), None)
+
+    assert call(8, 2, 64) == 1                        # prefill block size
+    assert call(8, 2, 0) == 1
+    assert call(8, 2, 16, flags=8) == 1               # A_SORTED
+    assert call(8, 2, 16, flags=16) == 1              # OUT_SORTED
+    assert call(8, 2, 32, flags=32) == 1              # SPLIT
+    assert call(1025, 4, 16) == 2                     # 4100 routed rows > 4096
+    assert call(8, 2, 16, ids=None) == 1              # no ids
+    assert call(8, 2, 16, a_rows=9) == 1              # A rows must be the token count

@@ -82,6 +82,8 @@ _SIGNATURES = {
     "moe_w4a16_contiguous": (_I, [_P, _I, _I, _P, ctypes.POINTER(Desc), _P, _P, _I, _I, _P, _U32, _P, _P, _SZ, _P]),
     "moe_w4a16_masked": (_I, [_P, _I, _I, _I, _P, _I, ctypes.POINTER(Desc), _P, _P, _I, _I, _P, _U32, _P, _P, _SZ,
                               _P]),
+    "moe_w4a16_indexed_routed": (_I, [_P, _I, _I, ctypes.POINTER(Desc), _P, _P, _I, _I, _I, _P, _U32, _P, _P, _SZ,
+                                      _P]),
     "moe_w4a16_indexed_noalloc": (_I, [_P, _I, _I, ctypes.POINTER(Desc), _P, _P, _P, _P, _I, _I, _I, _P, _U32, _P,
                                        ctypes.POINTER(_P), _P]),
 }
@@ -395,6 +397,30 @@ def indexed(a: torch.Tensor, pw: PreparedWeight, sorted_ids: torch.Tensor, exper
                                       _ptr(sorted_ids), _ptr(expert_ids), _ptr(num_post_padded), num_tokens, top_k,
                                       block_m, _ptr(topk_weights), flags, _ptr(out), _ptr(ws), ws.numel(),
                                       _stream(dev)), "indexed")
+    return out
+
+
+ROUTED_MAX_ROWS = 4096   # routed rows (T * top_k) of one indexed_routed call
+
+
+def indexed_routed(a: torch.Tensor, pw: PreparedWeight, topk_ids: torch.Tensor, block_m: int, ws: torch.Tensor,
+                   flags: int = 0, topk_weights: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """moe_w4a16_indexed_routed: the decode-kernel indexed GEMM from the router's topk_ids [T, top_k] in one
+    launch (each CTA builds the align step's block layout itself); same output as align + indexed."""
+    dev = pw.buffer.device
+    _need(a, "a", _BF16, dev)
+    _need(topk_ids, "topk_ids", _I32, dev)
+    if topk_weights is not None:
+        _need(topk_weights, "topk_weights", (torch.float32,), dev)
+    num_tokens, top_k = topk_ids.shape
+    rows = num_tokens if flags & FLAG_COMBINE else num_tokens * top_k
+    if out is None:
+        out = torch.empty((rows, _out_cols(pw, flags)), dtype=torch.bfloat16, device=dev)
+    with torch.cuda.device(dev):
+        _check(_lib.moe_w4a16_indexed_routed(_ptr(a), a.shape[0], a.shape[1], ctypes.byref(pw.desc), _ptr(pw.buffer),
+                                             _ptr(topk_ids), num_tokens, top_k, block_m, _ptr(topk_weights), flags,
+                                             _ptr(out), _ptr(ws), ws.numel(), _stream(dev)), "indexed_routed")
     return out
 
 

@@ -645,6 +645,38 @@ moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, int k, const m
   return run_gemm(p, kernel, num_tokens, s);
 }
 
+moe_w4a16_status moe_w4a16_indexed_routed(const uint16_t* a, int a_rows, int k, const moe_w4a16_desc* desc,
+                                          const void* prepared, const int32_t* topk_ids, int num_tokens, int top_k,
+                                          int block_m, const float* topk_weights, uint32_t flags, uint16_t* c,
+                                          void* ws, size_t ws_bytes, moe_w4a16_stream_t stream) {
+  if (block_m < 1 || block_m > kDecodeRows) return MOE_W4A16_ERR_INVALID_ARG;
+  if (flags & (MOE_W4A16_FLAG_A_SORTED | MOE_W4A16_FLAG_OUT_SORTED | MOE_W4A16_FLAG_SPLIT))
+    return MOE_W4A16_ERR_INVALID_ARG;
+  WsLayout L;
+  moe_w4a16_status st = check_gemm_common(MOE_W4A16_LAYOUT_INDEXED, block_m, desc, prepared, a, k, flags, topk_weights,
+                                          num_tokens, top_k, c, ws, ws_bytes, &L, num_tokens == 0);
+  if (st != MOE_W4A16_OK) return st;
+  const int64_t r = static_cast<int64_t>(num_tokens) * top_k;
+  if (r > kRoutedMaxRows) return MOE_W4A16_ERR_UNSUPPORTED;
+  if (topk_ids == nullptr && r > 0) return MOE_W4A16_ERR_INVALID_ARG;
+  const bool per_row = flags & MOE_W4A16_FLAG_A_PER_ROW;
+  if (a_rows != (per_row ? r : num_tokens)) return MOE_W4A16_ERR_INVALID_ARG;
+  if (r == 0) return MOE_W4A16_OK;
+  size_t ms, mb;
+  st = moe_w4a16_align_size(num_tokens, top_k, static_cast<int>(desc->num_experts), block_m, &ms, &mb);
+  if (st != MOE_W4A16_OK) return st;
+  GemmParams p;
+  fill_common(p, desc, prepared, a, k, flags, topk_weights, num_tokens, top_k, c, ws, L);
+  p.layout = MOE_W4A16_LAYOUT_INDEXED;
+  p.a_rows = a_rows;
+  p.topk_ids = topk_ids;
+  p.block_m = block_m;
+  p.sorted_cap = static_cast<int64_t>(ms);
+  p.a_div = per_row ? 1 : top_k;
+  p.c_rows = r;
+  return run_gemm(p, MOE_W4A16_KERNEL_DECODE, num_tokens, reinterpret_cast<cudaStream_t>(stream));
+}
+
 moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad, int k, const int32_t* m_indices,
                                       const moe_w4a16_desc* desc, const void* prepared, const int32_t* row_ids,
                                       int num_tokens, int top_k, const float* topk_weights, uint32_t flags,

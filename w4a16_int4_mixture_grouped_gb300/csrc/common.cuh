@@ -67,6 +67,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // limit is what ends them.
 constexpr uint32_t kSuspendNs = 20000u;
 
+// The wait limit of a kernel instantiation: the fixed default, or (diagnostic instantiations,
+// launched only while the host has lowered the limit) the launch's own GemmParams::wait_ns.
+template <bool DIAG>
+__device__ __forceinline__ uint64_t wait_limit(const GemmParams& p) {
+  return DIAG ? p.wait_ns : kWaitLimitNs;
+}
+
 // try_wait that may suspend the thread for up to `hint_ns` while the phase is incomplete.
 __device__ __forceinline__ bool mbar_test_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;

@@ -57,6 +57,7 @@ enum { kRecIdx = 0, kRecGroup, kRecChunks, kRecPart, kRecCut, kRecTiles, kRecMet
 constexpr int kRecInts = kRecMeta + 2 * 32;
 constexpr int kRecBytes = kStages * kRecInts * 4;
 constexpr int kSlices = kConsumerWarps;                 // combine counter slices per group
+static_assert(kStages * (2 * kChunkBytes) >= 2 * kRoutedMaxRows, "routed ids fit in the stage ring");
 
 // Geometry of the kernel variant whose row blocks hold up to ROWS (16 or 32)
 // routed rows. The 16-row variant's smaller stages and accumulators (72
@@ -102,7 +103,7 @@ __device__ __forceinline__ void store_bf16(uint16_t* base, int64_t idx, float v)
 // stage, a lane loads its four FU words of each chunk, its scales, and the
 // activation B fragments of NT tiles, releases the stage, then dequantises
 // 8 FUs and issues 8*NT MMAs. Returns false when a wait gave up.
-template <int ROWS, int NT>
+template <int ROWS, int NT, bool DIAG>
 __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s, int& stage, uint32_t& phase,
                                              uint32_t wq_off, uint32_t sc_off, int lane, int nkc,
                                              float (&acc)[2][Geo<ROWS>::kTiles][4], PipeStats& ps) {
@@ -115,7 +116,7 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
   const uint32_t act_lane = 2 * kChunkBytes + (lane & 7) * kActStride + (lane >> 3) * 16;
   for (int kc = 0; kc < nkc; ++kc) {
     ps.start();
-    if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err, p.wait_ns)) return false;
+    if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err, wait_limit<DIAG>(p))) return false;
     ps.stop(0);
     ps.add(1, 1);
     const uint32_t sb = s.stages + stage * Geo<ROWS>::kStageBytes;
@@ -247,7 +248,8 @@ __device__ __forceinline__ bool part_fixup(const GemmParams& p, int su, int part
   return true;
 }
 
-template <int ROWS>
+// DIAG: the diagnostic instantiation, whose waits take the launch's own limit (moe_w4a16_set_wait_limit_ns).
+template <int ROWS, bool DIAG>
 __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_kernel(const GemmParams p) {
   using G = Geo<ROWS>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     fence_mbar_init();
   }
   if (p.layout == MOE_W4A16_LAYOUT_MASKED && warp == 0) masked_prefix_warp(p, ROWS, s.prefix);
-  if (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.hot == nullptr && warp == kConsumerWarps) {
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.hot == nullptr && p.topk_ids == nullptr && warp == kConsumerWarps) {
     // the first piece of this CTA is piece blockIdx.x; when that is a whole unit, its row block is
     // blockIdx.x / NG: warm L1 with the block's routing entries while the block count loads
     const int64_t blk0 = blockIdx.x / p.NG;
@@ -279,6 +281,9 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     }
   }
   __syncthreads();
+  // a routed call: every CTA builds the align step's block layout from the router's output itself
+  // (the stage ring, still unused, holds the ids meanwhile)
+  if (p.topk_ids != nullptr) route_in_smem(p, s.prefix, reinterpret_cast<uint16_t*>(smem));
 
   const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED ? p.block_m : ROWS;
   int nblk = num_row_blocks(p, rows_per_block, s.prefix);
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       int local;
       const int e = block_expert(p, blk, rows_per_block, s.prefix, local);
       if (e < 0) continue;
-      const RowRef rr = block_row(p, blk, e, local, rows_per_block, lane);
+      const RowRef rr = block_row(p, blk, e, local, rows_per_block, lane, s.prefix);
       const bool valid = rr.a_row >= 0;
       const unsigned vmask = __ballot_sync(0xffffffffu, valid);
       if (vmask == 0) continue;
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       const int kc0 = pc.kc0, kc1 = pc.kc1;
       for (int kc = kc0; kc < kc1; ++kc) {
         pps.start();
-        if (!warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err, p.wait_ns)) goto producer_done;
+        if (!warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err, wait_limit<DIAG>(p))) goto producer_done;
         pps.stop(0);
         pps.add(1, 1);
         const uint32_t full = s.full + 8 * stage;
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       }
     }
     // no more units: one stage carries the end mark (33 plain arrivals complete its phase)
-    if (warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err, p.wait_ns)) {
+    if (warp_wait(s.empty + 8 * stage, phase ^ 1u, s.abort_flag, p.err, wait_limit<DIAG>(p))) {
       if (lane == 0) {
         recs[stage * kRecInts + kRecIdx] = -1;
         mbar_arrive(s.full + 8 * stage);
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
     while (true) {
       cps.stop(3);   // epilogue of the previous unit (and unit bookkeeping)
       // the next piece is the one the producer put at the head of the current stage
-      if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err, p.wait_ns)) goto consumer_done;
+      if (!warp_wait(s.full + 8 * stage, phase, s.abort_flag, p.err, wait_limit<DIAG>(p))) goto consumer_done;
       const int* rec = recs + stage * kRecInts;
       if (rec[kRecIdx] < 0) break;
       const int gp = rec[kRecGroup], ntiles = rec[kRecTiles];
@@ -418,12 +423,13 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
       cps.start();
       const long long t_unit = clock64();
       switch (ntiles) {
-        case 1: ok = consume_unit<ROWS, 1>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
-        case 2: ok = consume_unit<ROWS, 2>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
+        case 1: ok = consume_unit<ROWS, 1, DIAG>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
+        case 2: ok = consume_unit<ROWS, 2, DIAG>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
         case 3:
-          ok = consume_unit<ROWS, (G::kTiles > 2 ? 3 : 2)>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps);
+          ok = consume_unit<ROWS, (G::kTiles > 2 ? 3 : 2), DIAG>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc,
+                                                                  cps);
           break;
-        default: ok = consume_unit<ROWS, G::kTiles>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
+        default: ok = consume_unit<ROWS, G::kTiles, DIAG>(p, s, stage, phase, wq_off, sc_off, lane, nkc, acc, cps); break;
       }
       cps.add(2, static_cast<unsigned long long>(clock64() - t_unit));
       cps.add(4, 1);
@@ -521,28 +527,32 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
 
 namespace decode {
 
-template <int ROWS>
+template <int ROWS, bool DIAG>
 cudaError_t launch_rows(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
   using G = Geo<ROWS>;
   const DeviceInfo& di = device_info(device);
-  const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
-  static bool attr_set[64] = {false};
+  const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1
+                             : p.topk_ids != nullptr        ? routed_table_words(p.num_experts, p.R)
+                                                            : 0;
+  static bool attr_set[64] = {false};   // one table per instantiation
   if (device >= 0 && device < 64 && !attr_set[device]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         G::smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
+    const int most = routed_table_words(MOE_W4A16_MAX_EXPERTS, kRoutedMaxRows);
+    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel<ROWS, DIAG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         G::smem_bytes(most > MOE_W4A16_MAX_EXPERTS + 1 ? most
+                                                                                        : MOE_W4A16_MAX_EXPERTS + 1));
     if (e != cudaSuccess) return e;
     attr_set[device] = true;
   }
   // upper bound of work units known on the host
   int64_t max_blocks;
-  if (p.layout == MOE_W4A16_LAYOUT_INDEXED) max_blocks = p.sorted_cap / p.block_m;
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED) max_blocks = p.sorted_cap / p.block_m;   // routed: the align capacity
   else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) max_blocks = p.m_pad / ROWS;
   else max_blocks = static_cast<int64_t>(p.num_experts) * ((p.max_m + ROWS - 1) / ROWS);
   const int64_t units = max_blocks * p.NG;
   int64_t grid = static_cast<int64_t>(di.sm_count) * G::kCtasPerSm;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  decode_gemm_kernel<ROWS><<<static_cast<int>(grid), kThreads, G::smem_bytes(prefix_entries), stream>>>(p);
+  decode_gemm_kernel<ROWS, DIAG><<<static_cast<int>(grid), kThreads, G::smem_bytes(prefix_entries), stream>>>(p);
   note_launch();
   if (grid_out) *grid_out = static_cast<int>(grid);
   return cudaGetLastError();
@@ -555,8 +565,11 @@ cudaError_t launch_rows(const GemmParams& p, int device, cudaStream_t stream, in
 cudaError_t launch_decode_gemm(const GemmParams& p, int device, cudaStream_t stream, int* grid_out) {
   const bool small = (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.block_m <= kDecodeRowsSmall) ||
                      (p.layout == MOE_W4A16_LAYOUT_MASKED && p.max_m <= kDecodeRowsSmall);
-  return small ? decode::launch_rows<kDecodeRowsSmall>(p, device, stream, grid_out)
-               : decode::launch_rows<kDecodeRows>(p, device, stream, grid_out);
+  if (p.wait_ns != kWaitLimitNs)
+    return small ? decode::launch_rows<kDecodeRowsSmall, true>(p, device, stream, grid_out)
+                 : decode::launch_rows<kDecodeRows, true>(p, device, stream, grid_out);
+  return small ? decode::launch_rows<kDecodeRowsSmall, false>(p, device, stream, grid_out)
+               : decode::launch_rows<kDecodeRows, false>(p, device, stream, grid_out);
 }
 
 }  // namespace moe

@@ -206,6 +206,8 @@ __device__ __forceinline__ int block_extent(const GemmParams& p, int blk, int e,
   return hi;
 }
 
+// DIAG: the diagnostic instantiation, whose waits take the launch's own limit (moe_w4a16_set_wait_limit_ns).
+template <bool DIAG>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_gemm_kernel(const GemmParams p, const __grid_constant__ XMaps xmaps) {
   // a split call without experts above the decode kernel's rows: nothing to do (before any
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ok = 1;
         if (lane == 0) {
           ps.start();
-          ok = mbar_wait(p_empty + 8 * stage, phase ^ 1u, abort_flag, p.err, p.wait_ns);
+          ok = mbar_wait(p_empty + 8 * stage, phase ^ 1u, abort_flag, p.err, wait_limit<DIAG>(p));
           ps.stop(0);
           if (ok) {
             const uint32_t full = p_full + 8 * stage;
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16(128, nr);
       if (lane == 0) {
         ps.start();
-        bool ok = mbar_wait(acc_empty, aph ^ 1u, abort_flag, p.err, p.wait_ns);
+        bool ok = mbar_wait(acc_empty, aph ^ 1u, abort_flag, p.err, wait_limit<DIAG>(p));
         ps.stop(0);
         tc_fence_after();
         // A thread issues MMAs back to back every ~59 cycles, but each commit (~44) and each
@@ -338,8 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kc = 0; ok && kc < p.KC; ++kc) {
           ps.start();
           const uint32_t xf = x_full + 8 * xs, wf = w_full + 8 * ws;
-          if (!(p.wait_ns >= kSuspendNs && mbar_test(xf, xph) && mbar_test(wf, wph)))
-            ok = mbar_wait(xf, xph, abort_flag, p.err, p.wait_ns) && mbar_wait(wf, wph, abort_flag, p.err, p.wait_ns);
+          if (!(wait_limit<DIAG>(p) >= kSuspendNs && mbar_test(xf, xph) && mbar_test(wf, wph)))
+            ok = mbar_wait(xf, xph, abort_flag, p.err, wait_limit<DIAG>(p)) && mbar_wait(wf, wph, abort_flag, p.err, wait_limit<DIAG>(p));
           ps.stop(1);
           ps.add(3, 1);
           if (!ok) break;
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = block_row(p, blk, e, local, rows_per_block, 0).a_row;
       for (int kc = 0; kc < p.KC; ++kc) {
         ps.start();
-        if (!warp_wait(x_empty + 8 * stage, phase ^ 1u, abort_flag, p.err, p.wait_ns)) goto x_done;
+        if (!warp_wait(x_empty + 8 * stage, phase ^ 1u, abort_flag, p.err, wait_limit<DIAG>(p))) goto x_done;
         ps.stop(0);
         const uint32_t full = x_full + 8 * stage;
         if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nr) * 128u);
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         pst.start();
-        if (!warp_wait(p_full + 8 * ps, pph, abort_flag, p.err, p.wait_ns)) goto d_done;
+        if (!warp_wait(p_full + 8 * ps, pph, abort_flag, p.err, wait_limit<DIAG>(p))) goto d_done;
         pst.stop(0);
         const uint32_t pa = sbase + kPOff + ps * kPBytes + dq_tile * kChunkBytes;
         uint4 wv[2];
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pst.start();
         // the weight stage of chunk gch is free once both issuers' MMAs of chunk gch - kWStages
         // have completed
-        if (!warp_wait(w_empty + 8 * ws, ((gch / kWStages) & 1u) ^ 1u, abort_flag, p.err, p.wait_ns)) goto d_done;
+        if (!warp_wait(w_empty + 8 * ws, ((gch / kWStages) & 1u) ^ 1u, abort_flag, p.err, wait_limit<DIAG>(p))) goto d_done;
         pst.stop(1);
         pst.start();
         // A operand of this tile: TMEM lanes = channels (this warp's quarter), columns = k pairs of
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ------------------------------------------------- epilogue
       pst.start();
-      if (!warp_wait(acc_full, aph, abort_flag, p.err, p.wait_ns)) goto d_done;
+      if (!warp_wait(acc_full, aph, abort_flag, p.err, wait_limit<DIAG>(p))) goto d_done;
       pst.stop(3);
       pst.start();
       aph ^= 1u;
@@ -624,12 +626,14 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
   const DeviceInfo& di = device_info(device);
   const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
   const int smem = smem_bytes(prefix_entries);
-  static bool attr_set[64] = {false};
-  if (device >= 0 && device < 64 && !attr_set[device]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool diag = p.wait_ns != kWaitLimitNs;
+  static bool attr_set[2][64] = {{false}};
+  if (device >= 0 && device < 64 && !attr_set[diag][device]) {
+    cudaError_t e = cudaFuncSetAttribute(diag ? prefill_gemm_kernel<true> : prefill_gemm_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
     if (e != cudaSuccess) return e;
-    attr_set[device] = true;
+    attr_set[diag][device] = true;
   }
   int64_t max_blocks;
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED) max_blocks = p.cblocks != nullptr ? p.cb_cap : p.sorted_cap / p.block_m;
@@ -639,7 +643,10 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
   int64_t grid = di.sm_count;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  prefill_gemm_kernel<<<static_cast<int>(grid), kThreads, smem, stream>>>(p, xmaps);
+  if (diag)
+    prefill_gemm_kernel<true><<<static_cast<int>(grid), kThreads, smem, stream>>>(p, xmaps);
+  else
+    prefill_gemm_kernel<false><<<static_cast<int>(grid), kThreads, smem, stream>>>(p, xmaps);
   note_launch();
   if (grid_out) *grid_out = static_cast<int>(grid);
   return cudaGetLastError();

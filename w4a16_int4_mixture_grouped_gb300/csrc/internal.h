@@ -56,6 +56,7 @@ struct GemmParams {
   int layout;                // MOE_W4A16_LAYOUT_*
 
   // indexed
+  const int32_t* topk_ids;   // routed calls: the router's output; each CTA builds the block layout from it
   const int32_t* sorted_ids;
   const int32_t* expert_ids;
   const int32_t* num_post_padded;
@@ -167,5 +168,10 @@ constexpr int kSplitMaxTokE = 64;
 // Entries of the split's block table for R routed rows: every hot expert has more than kSplitRows rows.
 constexpr int64_t split_table_cap(int64_t R) { return R / kPrefillRows + R / (kSplitRows + 1) + 1; }
 constexpr int kMaxContigSegs = 2048;   // merged contiguous blocks: at most 2048 segments (262144 rows)
+// Routed calls (moe_w4a16_indexed_routed): the block layout a CTA keeps in shared memory, in 32-bit
+// words: a 32-bit count per expert, then 16-bit first rows and first blocks per expert (E + 1 each)
+// and the R routed rows' flat ids in expert order (16-bit).
+constexpr int kRoutedMaxRows = MOE_W4A16_ROUTED_MAX_ROWS;
+constexpr int routed_table_words(int E, int R) { return E + (2 * (E + 1) + R + 1) / 2; }
 
 }  // namespace moe

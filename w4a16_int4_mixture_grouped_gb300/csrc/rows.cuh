@@ -23,6 +23,94 @@
 
 namespace moe {
 
+// Routed calls: the block layout that moe_w4a16_align builds (experts in ascending order, each
+// expert's rows in ascending flat id, blocks of block_m), kept in a CTA's shared memory.
+struct RouteTab {
+  int* cnt;          // [E] routed rows per expert (then the placement cursors)
+  uint16_t* off;     // [E + 1] position of an expert's first row in `sorted`
+  uint16_t* bp;      // [E + 1] first block of an expert; bp[E] = blocks of the call
+  uint16_t* sorted;  // [R] flat ids t * top_k + j in expert order
+};
+__device__ __forceinline__ RouteTab route_tab(const GemmParams& p, const int* base) {
+  RouteTab t;
+  t.cnt = const_cast<int*>(base);
+  t.off = reinterpret_cast<uint16_t*>(t.cnt + p.num_experts);
+  t.bp = t.off + p.num_experts + 1;
+  t.sorted = t.bp + p.num_experts + 1;
+  return t;
+}
+
+// Builds the routed block layout from p.topk_ids in shared memory (every thread of the CTA calls it).
+// Ids outside [0, E) are skipped and recorded. The ids are read from global memory once, into
+// `ids16` (R 16-bit entries of shared memory the caller lends, 0xFFFF for a skipped id). The
+// placement is stable: one warp takes the flat ids in ascending order, 32 at a time, and ranks equal
+// experts within each group of 32 with match.any.
+static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* ids16) {
+  const RouteTab t = route_tab(p, base);
+  const int E = p.num_experts, R = p.R, bm = p.block_m;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) t.cnt[i] = 0;
+  __syncthreads();
+  for (int f = threadIdx.x; f < R; f += blockDim.x) {
+    const int e = p.topk_ids[f];
+    const bool ok = e >= 0 && e < E;
+    ids16[f] = ok ? static_cast<uint16_t>(e) : static_cast<uint16_t>(0xFFFFu);
+    if (ok) atomicAdd(t.cnt + e, 1);
+    else set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    // exclusive scans of rows and blocks over experts: lane l takes experts [l*per, (l+1)*per)
+    const int per = (E + 31) / 32;
+    int rows = 0, blocks = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        rows += t.cnt[e];
+        blocks += (t.cnt[e] + bm - 1) / bm;
+      }
+    }
+    int r_inc = rows, b_inc = blocks;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int r2 = __shfl_up_sync(0xffffffffu, r_inc, o), b2 = __shfl_up_sync(0xffffffffu, b_inc, o);
+      if (lane >= o) {
+        r_inc += r2;
+        b_inc += b2;
+      }
+    }
+    int r_run = r_inc - rows, b_run = b_inc - blocks;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        const int c = t.cnt[e];
+        t.off[e] = static_cast<uint16_t>(r_run);
+        t.bp[e] = static_cast<uint16_t>(b_run);
+        r_run += c;
+        b_run += (c + bm - 1) / bm;
+        t.cnt[e] = 0;   // now the placement cursor
+      }
+    }
+    if (lane == 31) {
+      t.off[E] = static_cast<uint16_t>(r_run);
+      t.bp[E] = static_cast<uint16_t>(b_run);
+    }
+    __syncwarp();
+    for (int b0 = 0; b0 < R; b0 += 32) {
+      const int f = b0 + lane;
+      const int e = f < R ? static_cast<int>(ids16[f]) : 0xFFFF;
+      const bool ok = e < E;
+      const unsigned m = __match_any_sync(0xffffffffu, ok ? e : E + lane);
+      const int rank = __popc(m & ((1u << lane) - 1u));
+      if (ok) t.sorted[t.off[e] + t.cnt[e] + rank] = static_cast<uint16_t>(f);
+      __syncwarp();
+      if (ok && rank == 0) t.cnt[e] += __popc(m);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+}
+
 // Builds prefix[e] = blocks of experts < e for the masked layout (warp 0 only).
 __device__ __forceinline__ void masked_prefix_warp(const GemmParams& p, int rows, int* prefix) {
   const int lane = threadIdx.x & 31;
@@ -57,6 +145,7 @@ __device__ __forceinline__ void masked_prefix_warp(const GemmParams& p, int rows
 // Number of row blocks of the call.
 __device__ __forceinline__ int num_row_blocks(const GemmParams& p, int rows, const int* prefix) {
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED) {
+    if (p.topk_ids != nullptr) return route_tab(p, prefix).bp[p.num_experts];
     if (p.cblocks != nullptr) {
       const int nb = p.cblocks[0].x;
       if (nb < 0 || nb > p.cb_cap) {
@@ -90,6 +179,16 @@ __device__ __forceinline__ int block_expert(const GemmParams& p, int blk, int ro
   local = 0;
   int e;
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED) {
+    if (p.topk_ids != nullptr) {
+      const RouteTab t = route_tab(p, prefix);
+      int lo = 0, hi = p.num_experts;  // largest e with bp[e] <= blk
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (t.bp[mid] <= blk) lo = mid; else hi = mid;
+      }
+      local = blk - t.bp[lo];
+      return lo;
+    }
     e = p.cblocks != nullptr ? p.cblocks[1 + blk].y : p.expert_ids[blk];
   } else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) {
     e = p.cblocks != nullptr ? p.cblocks[1 + blk].y : p.m_indices[static_cast<int64_t>(blk) * rows];
@@ -116,10 +215,25 @@ struct RowRef {
   int flat;     // flat routed-row id t*top_k + j (or -1)
 };
 
-// Row i of block blk (expert e, expert-local block index `local`).
-__device__ __forceinline__ RowRef block_row(const GemmParams& p, int blk, int e, int local, int rows, int i) {
+// Row i of block blk (expert e, expert-local block index `local`). `prefix` is the CTA's masked
+// prefix or routed table (shared memory).
+__device__ __forceinline__ RowRef block_row(const GemmParams& p, int blk, int e, int local, int rows, int i,
+                                            const int* prefix = nullptr) {
   RowRef r{-1, -1, -1};
-  if (p.layout == MOE_W4A16_LAYOUT_INDEXED) {
+  if (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.topk_ids != nullptr) {
+    const RouteTab t = route_tab(p, prefix);
+    const int idx = local * p.block_m + i;
+    if (i >= p.block_m || idx >= t.off[e + 1] - t.off[e]) return r;   // a padding row
+    const int f = t.sorted[t.off[e] + idx];
+    const int ar = f / p.a_div;
+    if (ar >= p.a_rows) {
+      set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
+      return r;
+    }
+    r.a_row = ar;
+    r.out_row = f;
+    r.flat = f;
+  } else if (p.layout == MOE_W4A16_LAYOUT_INDEXED) {
     int slot;
     if (p.cblocks != nullptr) {
       const int4 b = p.cblocks[1 + blk];
