@@ -441,14 +441,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t gch = 0;   // k-chunks this CTA has dequantised
     const bool swiglu = p.flags & MOE_W4A16_FLAG_SWIGLU;
     const bool combine = p.flags & MOE_W4A16_FLAG_COMBINE;
-    for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
-      int blk, gp;
-      unit_coords(p, nblk, u, blk, gp);
-      int local;
-      const int e = block_expert(p, blk, rows_per_block, prefix, local);
-      if (e < 0) continue;
-      const int ext = block_extent(p, blk, e, local, rows_per_block);
-      if (ext == 0) continue;
+    // The k-loop does not depend on a unit's rows, only the epilogue does: the next unit with work
+    // (its expert and row extent, a few dependent index loads) is looked up after this unit's last
+    // k-chunk, while its MMAs drain, instead of between the epilogue and the next k-loop.
+    struct DqUnit {
+      int64_t u;
+      int blk, gp, e, local, ext;
+    };
+    auto find_unit = [&](int64_t u) {
+      DqUnit x{u, 0, 0, -1, 0, 0};
+      for (; x.u < total_units; x.u += gridDim.x) {
+        unit_coords(p, nblk, x.u, x.blk, x.gp);
+        x.e = block_expert(p, x.blk, rows_per_block, prefix, x.local);
+        if (x.e < 0) continue;
+        x.ext = block_extent(p, x.blk, x.e, x.local, rows_per_block);
+        if (x.ext > 0) break;
+      }
+      return x;
+    };
+    for (DqUnit cur = find_unit(blockIdx.x); cur.u < total_units;) {
+      const int blk = cur.blk, gp = cur.gp, e = cur.e, local = cur.local, ext = cur.ext;
       const int nr = (ext + 15) & ~15;
       for (int kc = 0; kc < p.KC; ++kc) {
         // k-chunks alternate between the two groups of eight warps (half the barrier traffic of
@@ -518,6 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++ws == kWStages) ws = 0;
       }
 
+      const DqUnit nxt = find_unit(cur.u + gridDim.x);
+
       // ------------------------------------------------- epilogue
       pst.start();
       if (!warp_wait(acc_full, aph, abort_flag, p.err, wait_limit<DIAG>(p))) goto d_done;
@@ -568,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(acc_empty);
       pst.stop(4);
       pst.add(5, 1);
+      cur = nxt;
     }
   d_done:
     if (lane == 0) pst.flush(pipe_stats_ptr() + 24);
