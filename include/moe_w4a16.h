@@ -255,7 +255,7 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_gather_sorted(const uint16_t* src, int 
  * overrides the family (read on every call, part of the memo key). Indexed
  * block_m: 16 for the decode family at tok_e <= 4, 32 for the rest of the
  * decode family, 192 for the prefill family. Indexed calls with
- * 8 <= tok_e < 64 (without a forced family) get MOE_W4A16_KERNEL_SPLIT with
+ * 8 <= tok_e < 128 (without a forced family) get MOE_W4A16_KERNEL_SPLIT with
  * block_m 32: under skewed routing such calls mix experts of a few rows and
  * experts of hundreds, and each family serves its own (the caller passes
  * MOE_W4A16_FLAG_SPLIT; a call that also combines uses the decode family).

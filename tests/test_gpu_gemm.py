@@ -322,10 +322,11 @@ def test_mode_mismatch_fails_before_launch():
 
 @pytest.mark.parametrize("tokens,kernel,block_m,masked_kernel",
                          [(16, 1, 16, 1), (128, 1, 16, 1), (192, 1, 16, 1), (256, 1, 32, 1), (512, 3, 32, 1),
-                          (1536, 3, 32, 2), (3072, 2, 192, 2), (8192, 2, 192, 2)])
+                          (1536, 3, 32, 2), (3072, 3, 32, 2), (6096, 3, 32, 2), (6144, 2, 192, 2),
+                          (8192, 2, 192, 2)])
 def test_plan_picks_family_and_block_from_rows_per_expert(tokens, kernel, block_m, masked_kernel):
     """tok_e = T*top_k/E (384 experts, top-8): decode 16-row blocks up to 4 rows per expert, decode 32-row blocks
-    below 8, the split per expert (indexed) from 8 to 63, the tcgen05 family from 64 on; masked calls switch
+    below 8, the split per expert (indexed) from 8 to 127, the tcgen05 family from 128 on; masked calls switch
     from the decode to the tcgen05 family at 24 rows per expert."""
     s = M.plan(M.LAYOUT_INDEXED, tokens, 8, 384, 4096, 7168)
     assert (s.kernel, s.block_m) == (kernel, block_m)
