@@ -367,12 +367,14 @@ def test_cut_units_match_the_oracle(e, t, k, kd, flags, regime):
 SPLIT_COUNTS = [1, 5, 31, 32, 33, 0, 64, 191, 192, 193, 400, 2]
 
 
-@pytest.mark.parametrize("counts", [SPLIT_COUNTS, [3, 7, 32, 0, 12], [33, 200, 385]])
-@pytest.mark.parametrize("block_m", [16, 32])
+@pytest.mark.parametrize("counts", [SPLIT_COUNTS, [3, 7, 32, 0, 12], [33, 200, 385], [224, 225, 416, 384, 40]])
+@pytest.mark.parametrize("block_m", [16, 20, 32])
 def test_split_matches_oracle(counts, block_m):
     """FLAG_SPLIT: experts above 32 rows on the tcgen05 kernel (blocks of up to 192 of their rows), the others on
-    the decode kernel; rows around 32 and the 192-row block edges, no hot expert, only hot experts; repeats are
-    bit-identical."""
+    the decode kernel, and so are the rows of a hot expert past its last full 192-row block when they are at
+    most 32 (224, 416: exactly 32; 225: 33 stay on the tcgen05 kernel) and start on a decode block boundary
+    (block_m 20: never, everything of a hot expert stays); rows around 32 and the 192-row block edges, no hot
+    expert, only hot experts; repeats are bit-identical."""
     rng = np.random.default_rng(800 + sum(counts) + block_m)
     e, kd, n = len(counts), 256, 512
     ids = ids_from_counts(rng, counts)

@@ -398,6 +398,7 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
                                                              int* err) {
   __shared__ int cnt[MOE_W4A16_MAX_EXPERTS];
   __shared__ int first[MOE_W4A16_MAX_EXPERTS];
+  __shared__ int cold_from[MOE_W4A16_MAX_EXPERTS];   // an expert's first block the decode side takes
   __shared__ int wsum[32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   for (int e = t; e < E; e += blockDim.x) {
@@ -429,8 +430,16 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
   const int e = t;
   const int c = e < E ? cnt[e] : 0;
   const bool is_hot = c > kSplitRows;
-  const int nbk = is_hot ? (c + kPrefillRows - 1) / kPrefillRows : 0;
-  if (e < E) hot[e] = is_hot ? 1 : 0;
+  // a hot expert's rows past its last full kPrefillRows block, when they are no more than a
+  // decode block's and start on a block boundary, go to the decode side too: a tcgen05 unit
+  // costs the same whatever its rows, so a few-row remainder block is better streamed there
+  const int full = c / kPrefillRows, rem = c - full * kPrefillRows;
+  const bool rem_cold = is_hot && full > 0 && rem > 0 && rem <= kSplitRows && kPrefillRows % block_m == 0;
+  const int nbk = is_hot ? (rem_cold ? full : (c + kPrefillRows - 1) / kPrefillRows) : 0;
+  if (e < E) {
+    hot[e] = is_hot ? (rem_cold ? 2 : 1) : 0;
+    cold_from[e] = !is_hot ? 0 : (rem_cold ? full * (kPrefillRows / block_m) : 0x7fffffff);
+  }
   int incl = nbk;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -461,8 +470,9 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
     if (total > cap) set_error(err, MOE_W4A16_ERR_CAPACITY);
     table[0] = make_int4(total < cap ? total : cap, 0, 0, 0);
   }
-  // the decode side's blocks: the other experts' blocks in block order, after the flags
-  // (hot[E] = count, hot[E + 1 + i] = block), so the decode kernel hands out no unit it skips
+  // the decode side's blocks: the other experts' blocks (and the remainder blocks of hot experts) in
+  // block order, after the flags (hot[E] = count, hot[E + 1 + i] = block), so the decode kernel
+  // hands out no unit it skips
   int32_t* cold = hot + E;
   int carry = 0;
   for (int b0 = 0; b0 < nb; b0 += blockDim.x) {
@@ -471,7 +481,7 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
     int keep = 0;
     if (b < nb) {
       const int x = expert_ids[b];
-      keep = (x >= 0 && x < E && cnt[x] <= kSplitRows) ? 1 : 0;
+      keep = (x >= 0 && x < E && b - first[x] >= cold_from[x]) ? 1 : 0;
     }
     int inc = keep;
 #pragma unroll
