@@ -669,6 +669,10 @@ REGIMES = (["decode_gate_up", "decode_gate_up_masked", "decode_down_combine", "t
            + [f"sweep_gate_up_t{t}_{skew}" for t in S.SWEEP_TOKENS for skew in ("uniform", "zipf")])
 
 
+# decode workloads also timed as align + GEMM (two launches) beside the one-launch routed call
+TWO_LAUNCH_TOO = ("decode_gate_up", "decode_down_combine", "tp8_decode_gate_up")
+
+
 def host_overhead(arm, calls: int = 200):
     """Host time to issue one GEMM call of an indexed single-GEMM workload, GPU busy behind it: through the
     Python binding, and through the C entry point alone with pre-marshalled ctypes arguments."""
@@ -728,6 +732,18 @@ def measure_regimes(names, dev, steps: int, warmup: int, peaks, peaks_src, sampl
         rec["roofline"]["traffic"] = traffic
         if name == "decode_gate_up":
             rec["host_overhead"] = host_overhead(arm)
+        if getattr(arm, "routed", False) and name in TWO_LAUNCH_TOO:
+            # the same workload as align + GEMM (two launches): its GEMM alone against the roofline
+            del arm
+            arm2 = OurArm(wl, layout, dev, routed=False)
+            for _ in range(warmup):
+                arm2.step()
+            t_ms, d_us, n_l = time_steps(arm2, steps, torch.cuda.current_stream(dev), sampler)
+            r2 = roofline_of(arm2, d_us, peaks, peaks_src)
+            rec["two_launch"] = {"us_per_call": t_ms * 1e3 / steps, "gpu_launches": n_l, "kernel_us": d_us,
+                                 "frac": r2["frac"], "achieved": r2["achieved"], "unit": r2["unit"],
+                                 "what": "align kernel + indexed GEMM; kernel_us and frac are the GEMM's alone"}
+            arm = arm2
         out[name] = rec
         del arm
         torch.cuda.empty_cache()

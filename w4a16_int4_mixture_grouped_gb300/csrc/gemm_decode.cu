@@ -57,7 +57,8 @@ enum { kRecIdx = 0, kRecGroup, kRecChunks, kRecPart, kRecCut, kRecTiles, kRecMet
 constexpr int kRecInts = kRecMeta + 2 * 32;
 constexpr int kRecBytes = kStages * kRecInts * 4;
 constexpr int kSlices = kConsumerWarps;                 // combine counter slices per group
-static_assert(kStages * (2 * kChunkBytes) >= 2 * kRoutedMaxRows, "routed ids fit in the stage ring");
+static_assert(kStages * (2 * kChunkBytes) >= 2 * ((kConsumerWarps + 1) * MOE_W4A16_MAX_EXPERTS + kRoutedMaxRows),
+              "the routing scratch (per-warp counts and ids) fits in the stage ring");
 
 // Geometry of the kernel variant whose row blocks hold up to ROWS (16 or 32)
 // routed rows. The 16-row variant's smaller stages and accumulators (72
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, Geo<ROWS>::kCtasPerSm) decode_gemm_k
   }
   __syncthreads();
   // a routed call: every CTA builds the align step's block layout from the router's output itself
-  // (the stage ring, still unused, holds the ids meanwhile)
+  // (the stage ring, still unused, lends its memory to the sort meanwhile)
   if (p.topk_ids != nullptr) route_in_smem(p, s.prefix, reinterpret_cast<uint16_t*>(smem));
 
   const int rows_per_block = p.layout == MOE_W4A16_LAYOUT_INDEXED ? p.block_m : ROWS;

@@ -41,25 +41,45 @@ __device__ __forceinline__ RouteTab route_tab(const GemmParams& p, const int* ba
 }
 
 // Builds the routed block layout from p.topk_ids in shared memory (every thread of the CTA calls it).
-// Ids outside [0, E) are skipped and recorded. The ids are read from global memory once, into
-// `ids16` (R 16-bit entries of shared memory the caller lends, 0xFFFF for a skipped id). The
-// placement is stable: one warp takes the flat ids in ascending order, 32 at a time, and ranks equal
-// experts within each group of 32 with match.any.
-static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* ids16) {
+// Ids outside [0, E) are skipped and recorded. A stable counting sort: each warp takes a contiguous
+// slice of the flat ids and counts its experts (equal ids of a group of 32 merged with match.any);
+// per expert, the warps' counts are turned into each warp's first position; after the scans over
+// experts each warp places its slice in order. `scratch` is shared memory the caller lends for the
+// call's duration: per-warp counts [warps][E] and the ids [R], 16 bits each.
+static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* scratch) {
   const RouteTab t = route_tab(p, base);
   const int E = p.num_experts, R = p.R, bm = p.block_m;
-  for (int i = threadIdx.x; i < E; i += blockDim.x) t.cnt[i] = 0;
+  const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint16_t* hist = scratch;            // [nw][E]: counts, then each warp's first position within the expert
+  uint16_t* ids16 = scratch + nw * E;  // [R]: expert of each flat id (0xFFFF: out of range)
+  const int per_w = ((R + nw - 1) / nw + 31) & ~31;
+  const int f0 = min(R, warp * per_w), f1 = min(R, f0 + per_w);
+  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  for (int f = threadIdx.x; f < R; f += blockDim.x) {
-    const int e = p.topk_ids[f];
+  for (int b0 = f0; b0 < f1; b0 += 32) {
+    const int f = b0 + lane;
+    const int e = f < f1 ? p.topk_ids[f] : -1;
     const bool ok = e >= 0 && e < E;
-    ids16[f] = ok ? static_cast<uint16_t>(e) : static_cast<uint16_t>(0xFFFFu);
-    if (ok) atomicAdd(t.cnt + e, 1);
-    else set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
+    if (f < f1) {
+      ids16[f] = ok ? static_cast<uint16_t>(e) : static_cast<uint16_t>(0xFFFFu);
+      if (!ok) set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, ok ? e : E + lane);
+    if (ok && (m & ((1u << lane) - 1u)) == 0) hist[warp * E + e] += static_cast<uint16_t>(__popc(m));
+    __syncwarp();
   }
   __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < nw; ++w) {
+      const int h = hist[w * E + e];
+      hist[w * E + e] = static_cast<uint16_t>(run);
+      run += h;
+    }
+    t.cnt[e] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {
     // exclusive scans of rows and blocks over experts: lane l takes experts [l*per, (l+1)*per)
     const int per = (E + 31) / 32;
     int rows = 0, blocks = 0;
@@ -83,30 +103,28 @@ static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* i
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
       if (e < E) {
-        const int c = t.cnt[e];
         t.off[e] = static_cast<uint16_t>(r_run);
         t.bp[e] = static_cast<uint16_t>(b_run);
-        r_run += c;
-        b_run += (c + bm - 1) / bm;
-        t.cnt[e] = 0;   // now the placement cursor
+        r_run += t.cnt[e];
+        b_run += (t.cnt[e] + bm - 1) / bm;
       }
     }
     if (lane == 31) {
       t.off[E] = static_cast<uint16_t>(r_run);
       t.bp[E] = static_cast<uint16_t>(b_run);
     }
+  }
+  __syncthreads();
+  for (int b0 = f0; b0 < f1; b0 += 32) {
+    const int f = b0 + lane;
+    const int e = f < f1 ? static_cast<int>(ids16[f]) : 0xFFFF;
+    const bool ok = e < E;
+    const unsigned m = __match_any_sync(0xffffffffu, ok ? e : E + lane);
+    const int rank = __popc(m & ((1u << lane) - 1u));
+    if (ok) t.sorted[t.off[e] + hist[warp * E + e] + rank] = static_cast<uint16_t>(f);
     __syncwarp();
-    for (int b0 = 0; b0 < R; b0 += 32) {
-      const int f = b0 + lane;
-      const int e = f < R ? static_cast<int>(ids16[f]) : 0xFFFF;
-      const bool ok = e < E;
-      const unsigned m = __match_any_sync(0xffffffffu, ok ? e : E + lane);
-      const int rank = __popc(m & ((1u << lane) - 1u));
-      if (ok) t.sorted[t.off[e] + t.cnt[e] + rank] = static_cast<uint16_t>(f);
-      __syncwarp();
-      if (ok && rank == 0) t.cnt[e] += __popc(m);
-      __syncwarp();
-    }
+    if (ok && rank == 0) hist[warp * E + e] += static_cast<uint16_t>(__popc(m));
+    __syncwarp();
   }
   __syncthreads();
 }
