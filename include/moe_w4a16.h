@@ -272,9 +272,9 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int to
  * per (token, 256 output channels, slice) and a bf16 [num_tokens*top_k, n]
  * staging buffer for the routed rows; for calls that may run the decode kernel
  * (indexed block_m <= 32, masked), the FP32 partial tiles and counters of the
- * units it cuts into k-ranges: the last min(units, 152) units of a call with
- * at most 2048 (row block, 256-channel) units (152 units x 4 parts: 10.0 MB for
- * block_m <= 16, 19.9 MB for 32-row blocks and masked calls); with
+ * units it cuts into k-ranges: the last min(units, 304) units of a call with
+ * at most 2048 (row block, 256-channel) units (304 units x 4 parts: 19.9 MB for
+ * block_m <= 16, 39.9 MB for 32-row blocks and masked calls); with
  * MOE_W4A16_FLAG_SPLIT also the table of the tcgen05 kernel's blocks (int4
  * [1 + R/192 + R/33]), a per-expert int32 flag [num_experts] and the decode
  * kernel's block list (int32 [1 + max_blocks]).

@@ -75,11 +75,11 @@ def test_workspace_size(lib):
     out = ctypes.c_size_t(0)
     f = lib.moe_w4a16_workspace_size
     # decode-family calls (masked, indexed block_m <= 32): header + the partial tiles of the units the kernel
-    # cuts into 4 k-ranges (the last 152 units of a call with at most 2048 units: 152 units x 4 parts x 8
+    # cuts into 4 k-ranges (the last 304 units of a call with at most 2048 units: 304 units x 4 parts x 8
     # warps x 32 lanes x FP32 values, 16 for 16-row blocks, 32 for 32-row blocks and masked calls) + their
-    # arrival counters (152 x 8 int32)
-    cut16 = 152 * 4 * 8 * 16 * 32 * 4 + 152 * 8 * 4
-    cut32 = 152 * 4 * 8 * 32 * 32 * 4 + 152 * 8 * 4
+    # arrival counters (304 x 8 int32)
+    cut16 = 304 * 4 * 8 * 16 * 32 * 4 + 304 * 8 * 4
+    cut32 = 304 * 4 * 8 * 32 * 32 * 4 + 304 * 8 * 4
     assert f(2, 128, 8, 384, 7168, 2048, 0, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut32
     assert f(0, 128, 8, 384, 7168, 2048, 32, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut32
     assert f(0, 64, 8, 384, 4096, 7168, 16, 0, ctypes.byref(out)) == 0 and out.value == 256 + cut16

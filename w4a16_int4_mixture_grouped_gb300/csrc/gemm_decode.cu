@@ -167,7 +167,8 @@ __device__ __forceinline__ bool consume_unit(const GemmParams& p, const Smem& s,
 // at most kCutUnitLimit units, its last min(units, kMaxCutUnits) units cut into
 // kParts k-ranges each. With a few units per SM the SMs that take one unit more than
 // the others set the end (measured: 8 of 152 SMs ran a sixth 56 us unit of the
-// 768-unit decode gate_up); quarter units at the end even them out. A call with
+// 768-unit decode gate_up); quarter units at the end even them out (the last 304,
+// two per SM: 199.5 -> 198.5 us there; 456 or eight parts were slower). A call with
 // fewer units than SMs (a narrow output such as one tensor-parallel shard's gate_up;
 // the Chord page, section "H200 prefill and TP8", tiles TP8 more flatly for the same
 // reason) has every unit cut, so that more CTAs stream weights. A cut unit is summed

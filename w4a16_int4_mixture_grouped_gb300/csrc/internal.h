@@ -139,8 +139,14 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
 
 // Decode: a call with at most kCutUnitLimit (row block, 256-channel group) units has its
 // last min(units, kMaxCutUnits) units cut into kParts k-ranges.
-constexpr int kParts = 4;
-constexpr int kMaxCutUnits = 152;
+#ifndef MOE_W4A16_DECODE_PARTS
+#define MOE_W4A16_DECODE_PARTS 4
+#endif
+#ifndef MOE_W4A16_DECODE_CUT_UNITS
+#define MOE_W4A16_DECODE_CUT_UNITS 304
+#endif
+constexpr int kParts = MOE_W4A16_DECODE_PARTS;
+constexpr int kMaxCutUnits = MOE_W4A16_DECODE_CUT_UNITS;
 constexpr int kCutUnitLimit = 2048;
 // Bytes of the cut-unit partial tiles for blocks of `rows` rows (16 or 32) and of their counters.
 constexpr size_t cut_partial_bytes(int rows) {

@@ -54,11 +54,19 @@ static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* s
   uint16_t* ids16 = scratch + nw * E;  // [R]: expert of each flat id (0xFFFF: out of range)
   const int per_w = ((R + nw - 1) / nw + 31) & ~31;
   const int f0 = min(R, warp * per_w), f1 = min(R, f0 + per_w);
+  // the first kRouteIdRegs x 32 id loads of this warp's slice are issued at once (one memory latency,
+  // overlapping the zeroing below, instead of one per 32 ids); with at most 4096 rows over the decode
+  // kernel's nine warps a slice has at most 480 ids, and any rest is loaded 32 at a time after them
+  constexpr int kRouteIdRegs = 16;
+  int ev[kRouteIdRegs];
+#pragma unroll
+  for (int j = 0; j < kRouteIdRegs; ++j) {
+    const int f = f0 + 32 * j + lane;
+    ev[j] = f < f1 ? __ldg(p.topk_ids + f) : -1;
+  }
   for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  for (int b0 = f0; b0 < f1; b0 += 32) {
-    const int f = b0 + lane;
-    const int e = f < f1 ? p.topk_ids[f] : -1;
+  auto count = [&](int f, int e) {
     const bool ok = e >= 0 && e < E;
     if (f < f1) {
       ids16[f] = ok ? static_cast<uint16_t>(e) : static_cast<uint16_t>(0xFFFFu);
@@ -67,6 +75,13 @@ static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* s
     const unsigned m = __match_any_sync(0xffffffffu, ok ? e : E + lane);
     if (ok && (m & ((1u << lane) - 1u)) == 0) hist[warp * E + e] += static_cast<uint16_t>(__popc(m));
     __syncwarp();
+  };
+#pragma unroll
+  for (int j = 0; j < kRouteIdRegs; ++j)
+    if (f0 + 32 * j < f1) count(f0 + 32 * j + lane, ev[j]);
+  for (int b0 = f0 + 32 * kRouteIdRegs; b0 < f1; b0 += 32) {
+    const int f = b0 + lane;
+    count(f, f < f1 ? __ldg(p.topk_ids + f) : -1);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -82,12 +97,18 @@ static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* s
   if (warp == 0) {
     // exclusive scans of rows and blocks over experts: lane l takes experts [l*per, (l+1)*per)
     const int per = (E + 31) / 32;
+    // ceil(c / bm) as a multiply-high by ceil(2^32 / bm): exact for c + bm - 1 < 2^32 / bm, far above
+    // the at most 4096 + 31 it sees here
+    const uint64_t inv = ((1ull << 32) + bm - 1) / bm;
+    auto blocks_of = [&](int c) {
+      return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(c + bm - 1)) * inv) >> 32);
+    };
     int rows = 0, blocks = 0;
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
       if (e < E) {
         rows += t.cnt[e];
-        blocks += (t.cnt[e] + bm - 1) / bm;
+        blocks += blocks_of(t.cnt[e]);
       }
     }
     int r_inc = rows, b_inc = blocks;
@@ -106,7 +127,7 @@ static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* s
         t.off[e] = static_cast<uint16_t>(r_run);
         t.bp[e] = static_cast<uint16_t>(b_run);
         r_run += t.cnt[e];
-        b_run += (t.cnt[e] + bm - 1) / bm;
+        b_run += blocks_of(t.cnt[e]);
       }
     }
     if (lane == 31) {
