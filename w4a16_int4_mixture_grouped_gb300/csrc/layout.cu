@@ -396,14 +396,16 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
                                                              int block_m, int R, int E, int cap,
                                                              int4* __restrict__ table, int32_t* __restrict__ hot,
                                                              int* err) {
-  __shared__ int cnt[MOE_W4A16_MAX_EXPERTS];
-  __shared__ int first[MOE_W4A16_MAX_EXPERTS];
-  __shared__ int cold_from[MOE_W4A16_MAX_EXPERTS];   // an expert's first block the decode side takes
+  __shared__ int first[MOE_W4A16_MAX_EXPERTS];      // an expert's first and last block
+  __shared__ int last[MOE_W4A16_MAX_EXPERTS];
+  __shared__ int last_rows[MOE_W4A16_MAX_EXPERTS];  // valid rows of its last block
+  __shared__ int cold_from[MOE_W4A16_MAX_EXPERTS];  // an expert's first block the decode side takes
   __shared__ int wsum[32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   for (int e = t; e < E; e += blockDim.x) {
-    cnt[e] = 0;
     first[e] = 0x7fffffff;
+    last[e] = -1;
+    last_rows[e] = 0;
   }
   __syncthreads();
   int n = *npp;
@@ -412,23 +414,34 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
     n = n < 0 ? 0 : static_cast<int>(sorted_cap);
   }
   const int nb = n / block_m;
+  // In the align layout an expert's blocks are consecutive and only its last one holds padding (the
+  // table below takes its rows as consecutive slots from its first block on), so its row count is
+  // block_m per block before the last plus the valid ids of the last: only last blocks are read.
+  const bool vec = block_m % 4 == 0 && (reinterpret_cast<uintptr_t>(sorted_ids) & 15) == 0;   // 16-byte aligned
   for (int b = t; b < nb; b += blockDim.x) {
     const int e = expert_ids[b];
     if (e < 0 || e >= E) {
       set_error(err, MOE_W4A16_ERR_BAD_INDEX);
       continue;
     }
+    if (b == 0 || expert_ids[b - 1] != e) first[e] = b;
+    if (b + 1 < nb && expert_ids[b + 1] == e) continue;
     int v = 0;
-    for (int i = 0; i < block_m; ++i) {
-      const int id = sorted_ids[static_cast<int64_t>(b) * block_m + i];
-      v += (id >= 0 && id < R) ? 1 : 0;
+    const int32_t* ids = sorted_ids + static_cast<int64_t>(b) * block_m;
+    if (vec) {
+      for (int i = 0; i < block_m; i += 4) {
+        const int4 q = *reinterpret_cast<const int4*>(ids + i);
+        v += (q.x >= 0 && q.x < R) + (q.y >= 0 && q.y < R) + (q.z >= 0 && q.z < R) + (q.w >= 0 && q.w < R);
+      }
+    } else {
+      for (int i = 0; i < block_m; ++i) v += (ids[i] >= 0 && ids[i] < R) ? 1 : 0;
     }
-    atomicAdd(&cnt[e], v);
-    atomicMin(&first[e], b);
+    last[e] = b;
+    last_rows[e] = v;
   }
   __syncthreads();
   const int e = t;
-  const int c = e < E ? cnt[e] : 0;
+  const int c = e < E && last[e] >= first[e] ? (last[e] - first[e]) * block_m + last_rows[e] : 0;
   const bool is_hot = c > kSplitRows;
   // a hot expert's rows past its last full kPrefillRows block, when they are no more than a
   // decode block's and start on a block boundary, go to the decode side too: a tcgen05 unit
