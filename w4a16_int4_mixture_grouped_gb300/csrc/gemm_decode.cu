@@ -57,8 +57,8 @@ enum { kRecIdx = 0, kRecGroup, kRecChunks, kRecPart, kRecCut, kRecTiles, kRecMet
 constexpr int kRecInts = kRecMeta + 2 * 32;
 constexpr int kRecBytes = kStages * kRecInts * 4;
 constexpr int kSlices = kConsumerWarps;                 // combine counter slices per group
-static_assert(kStages * (2 * kChunkBytes) >= 2 * ((kConsumerWarps + 1) * MOE_W4A16_MAX_EXPERTS + kRoutedMaxRows),
-              "the routing scratch (per-warp counts and ids) fits in the stage ring");
+static_assert(kStages * (2 * kChunkBytes) >= 2 * ((kConsumerWarps + 1) * MOE_W4A16_MAX_EXPERTS + kRoutedMaxRows + 1) + 256,
+              "the routing scratch (per-warp counts, ids, warp totals) fits in the stage ring");
 
 // Geometry of the kernel variant whose row blocks hold up to ROWS (16 or 32)
 // routed rows. The 16-row variant's smaller stages and accumulators (72

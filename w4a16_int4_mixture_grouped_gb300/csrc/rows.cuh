@@ -40,18 +40,35 @@ __device__ __forceinline__ RouteTab route_tab(const GemmParams& p, const int* ba
   return t;
 }
 
+// Lanes of the warp whose value v equals this lane's (v < 2^nbits): one ballot per bit of v, the
+// lanes agreeing with this lane on every bit. (match.any.sync gives the same mask; at a few hundred
+// experts it measured ~1.5k cycles per 32 ids on sm_103a, the ballots a few dozen.)
+__device__ __forceinline__ unsigned equal_lanes(int v, int nbits) {
+  unsigned m = 0xffffffffu;
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (v >> b) & 1;
+    const unsigned bal = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bal : ~bal;
+  }
+  return m;
+}
+
 // Builds the routed block layout from p.topk_ids in shared memory (every thread of the CTA calls it).
 // Ids outside [0, E) are skipped and recorded. A stable counting sort: each warp takes a contiguous
-// slice of the flat ids and counts its experts (equal ids of a group of 32 merged with match.any);
-// per expert, the warps' counts are turned into each warp's first position; after the scans over
-// experts each warp places its slice in order. `scratch` is shared memory the caller lends for the
-// call's duration: per-warp counts [warps][E] and the ids [R], 16 bits each.
+// slice of the flat ids and counts its experts (equal ids of a group of 32 merged through a ballot
+// mask); per expert, the warps' counts become each warp's first position, and one scan over the
+// experts (each thread a run of consecutive experts) gives every expert's first row and first block;
+// then each warp places its slice in order. `scratch` is shared memory the caller lends for the call's
+// duration: per-warp counts [warps][E] and the ids [R], 16 bits each, then 2 x 32 int32 of warp totals.
 static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* scratch) {
   const RouteTab t = route_tab(p, base);
   const int E = p.num_experts, R = p.R, bm = p.block_m;
   const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint16_t* hist = scratch;            // [nw][E]: counts, then each warp's first position within the expert
   uint16_t* ids16 = scratch + nw * E;  // [R]: expert of each flat id (0xFFFF: out of range)
+  int* wtot = reinterpret_cast<int*>(scratch + ((nw * E + R + 1) & ~1));   // [2][32]: warp totals of the scan
+  const int nbits = 32 - __clz(E + 31);   // ids and the per-lane stand-ins of invalid ones, E + lane < 2^nbits
+  const unsigned lt = (1u << lane) - 1u;
   const int per_w = ((R + nw - 1) / nw + 31) & ~31;
   const int f0 = min(R, warp * per_w), f1 = min(R, f0 + per_w);
   // the first kRouteIdRegs x 32 id loads of this warp's slice are issued at once (one memory latency,
@@ -72,8 +89,8 @@ static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* s
       ids16[f] = ok ? static_cast<uint16_t>(e) : static_cast<uint16_t>(0xFFFFu);
       if (!ok) set_error(p.err, MOE_W4A16_ERR_BAD_INDEX);
     }
-    const unsigned m = __match_any_sync(0xffffffffu, ok ? e : E + lane);
-    if (ok && (m & ((1u << lane) - 1u)) == 0) hist[warp * E + e] += static_cast<uint16_t>(__popc(m));
+    const unsigned m = equal_lanes(ok ? e : E + lane, nbits);
+    if (ok && (m & lt) == 0) hist[warp * E + e] += static_cast<uint16_t>(__popc(m));
     __syncwarp();
   };
 #pragma unroll
@@ -84,7 +101,18 @@ static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* s
     count(f, f < f1 ? __ldg(p.topk_ids + f) : -1);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  // ceil(c / bm) as a multiply-high by ceil(2^32 / bm) (bm >= 2): exact for c + bm - 1 < 2^32 / bm, far
+  // above the at most 4096 + 31 it sees here
+  const uint32_t inv = bm >= 2 ? 0xFFFFFFFFu / static_cast<uint32_t>(bm) + 1u : 0u;
+  auto blocks_of = [&](int c) {
+    return bm >= 2 ? static_cast<int>(__umulhi(static_cast<uint32_t>(c + bm - 1), inv)) : c;
+  };
+  // thread i takes experts [i q, i q + q): per expert, the warps' counts become their first positions
+  // and the expert's total; then an exclusive scan of the rows and blocks over the threads
+  const int q = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = min(E, static_cast<int>(threadIdx.x) * q), e1 = min(E, e0 + q);
+  int rows = 0, blocks = 0;
+  for (int e = e0; e < e1; ++e) {
     int run = 0;
     for (int w = 0; w < nw; ++w) {
       const int h = hist[w * E + e];
@@ -92,56 +120,45 @@ static __device__ void route_in_smem(const GemmParams& p, int* base, uint16_t* s
       run += h;
     }
     t.cnt[e] = run;
+    rows += run;
+    blocks += blocks_of(run);
+  }
+  int r_inc = rows, b_inc = blocks;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int r2 = __shfl_up_sync(0xffffffffu, r_inc, o), b2 = __shfl_up_sync(0xffffffffu, b_inc, o);
+    if (lane >= o) {
+      r_inc += r2;
+      b_inc += b2;
+    }
+  }
+  if (lane == 31) {
+    wtot[warp] = r_inc;
+    wtot[32 + warp] = b_inc;
   }
   __syncthreads();
-  if (warp == 0) {
-    // exclusive scans of rows and blocks over experts: lane l takes experts [l*per, (l+1)*per)
-    const int per = (E + 31) / 32;
-    // ceil(c / bm) as a multiply-high by ceil(2^32 / bm): exact for c + bm - 1 < 2^32 / bm, far above
-    // the at most 4096 + 31 it sees here
-    const uint64_t inv = ((1ull << 32) + bm - 1) / bm;
-    auto blocks_of = [&](int c) {
-      return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(c + bm - 1)) * inv) >> 32);
-    };
-    int rows = 0, blocks = 0;
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      if (e < E) {
-        rows += t.cnt[e];
-        blocks += blocks_of(t.cnt[e]);
-      }
-    }
-    int r_inc = rows, b_inc = blocks;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int r2 = __shfl_up_sync(0xffffffffu, r_inc, o), b2 = __shfl_up_sync(0xffffffffu, b_inc, o);
-      if (lane >= o) {
-        r_inc += r2;
-        b_inc += b2;
-      }
-    }
-    int r_run = r_inc - rows, b_run = b_inc - blocks;
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      if (e < E) {
-        t.off[e] = static_cast<uint16_t>(r_run);
-        t.bp[e] = static_cast<uint16_t>(b_run);
-        r_run += t.cnt[e];
-        b_run += blocks_of(t.cnt[e]);
-      }
-    }
-    if (lane == 31) {
-      t.off[E] = static_cast<uint16_t>(r_run);
-      t.bp[E] = static_cast<uint16_t>(b_run);
-    }
+  int r_run = r_inc - rows, b_run = b_inc - blocks;
+  for (int w = 0; w < warp; ++w) {
+    r_run += wtot[w];
+    b_run += wtot[32 + w];
+  }
+  for (int e = e0; e < e1; ++e) {
+    t.off[e] = static_cast<uint16_t>(r_run);
+    t.bp[e] = static_cast<uint16_t>(b_run);
+    r_run += t.cnt[e];
+    b_run += blocks_of(t.cnt[e]);
+  }
+  if (threadIdx.x == blockDim.x - 1) {   // its running sums are now the totals
+    t.off[E] = static_cast<uint16_t>(r_run);
+    t.bp[E] = static_cast<uint16_t>(b_run);
   }
   __syncthreads();
   for (int b0 = f0; b0 < f1; b0 += 32) {
     const int f = b0 + lane;
     const int e = f < f1 ? static_cast<int>(ids16[f]) : 0xFFFF;
     const bool ok = e < E;
-    const unsigned m = __match_any_sync(0xffffffffu, ok ? e : E + lane);
-    const int rank = __popc(m & ((1u << lane) - 1u));
+    const unsigned m = equal_lanes(ok ? e : E + lane, nbits);
+    const int rank = __popc(m & lt);
     if (ok) t.sorted[t.off[e] + hist[warp * E + e] + rank] = static_cast<uint16_t>(f);
     __syncwarp();
     if (ok && rank == 0) hist[warp * E + e] += static_cast<uint16_t>(__popc(m));
