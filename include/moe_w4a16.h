@@ -322,6 +322,7 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_clear_device_error(void* ws, moe_w4a16_
  *   a          bf16 [a_rows, k]: a_rows = T, or T*top_k with MOE_W4A16_FLAG_A_PER_ROW
  *   sorted_ids, expert_ids, num_post_padded: from moe_w4a16_align with this block_m
  *   block_m    1..32 runs the decode kernel (1..16: its 16-row variant), 33..192 the prefill kernel
+ *              (33..128: its 128-row variant, four weight stages in tensor memory instead of two)
  *   topk_weights float32 [T, top_k] (COMBINE only, else may be NULL)
  *   c          plain: bf16 [T*top_k, n] at row f; SWIGLU: [T*top_k, n/2]; COMBINE: [T, n] */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, int k, const moe_w4a16_desc* desc,

@@ -611,21 +611,23 @@ moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, int k, const m
   const int kernel = block_m <= kDecodeRows ? MOE_W4A16_KERNEL_DECODE : MOE_W4A16_KERNEL_PREFILL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (flags & MOE_W4A16_FLAG_SPLIT) {
-    // experts above kSplitRows rows: a table of their slots in blocks of up to 192 rows, their
-    // token rows copied to those slots, the tcgen05 kernel over the table; the decode kernel
+    // experts above kSplitRows rows: a table of their slots in blocks of up to kSplitTcRows rows,
+    // their token rows copied to those slots, the tcgen05 kernel over the table; the decode kernel
     // takes the other experts' blocks
     int4* table = reinterpret_cast<int4*>(static_cast<uint8_t*>(ws) + L.split_off);
     int32_t* hot = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + L.hot_off);
     uint16_t* g = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.gather_off);
-    MOE_CUDA_TRY(launch_split_table(sorted_ids, expert_ids, num_post_padded, p.sorted_cap, block_m, p.R,
-                                    p.num_experts, L.split_cap, table, hot, p.err, s));
-    MOE_CUDA_TRY(launch_gather_table(a, a_rows, k, sorted_ids, table, L.split_cap, p.R, p.a_div, g, p.err, s));
+    MOE_CUDA_TRY(launch_split_table(sorted_ids, expert_ids, num_post_padded, p.sorted_cap, block_m, kSplitTcRows,
+                                    p.R, p.num_experts, L.split_cap, table, hot, p.err, s));
+    MOE_CUDA_TRY(launch_gather_table(a, a_rows, k, sorted_ids, table, L.split_cap, kSplitTcRows, p.R, p.a_div, g,
+                                     p.err, s));
     GemmParams q = p;
     p.hot = hot;
     moe_w4a16_status st2 = run_gemm(p, MOE_W4A16_KERNEL_DECODE, num_tokens, s);
     if (st2 != MOE_W4A16_OK) return st2;
     q.cblocks = table;
     q.cb_cap = L.split_cap;
+    q.tc_rows = kSplitTcRows;
     q.a = g;
     q.a_rows = p.sorted_cap;
     q.a_div = 1;
@@ -642,6 +644,8 @@ moe_w4a16_status moe_w4a16_indexed(const uint16_t* a, int a_rows, int k, const m
     p.a_div = 1;
     p.a_sorted = 1;
   }
+  // blocks of at most 128 rows: the tcgen05 kernel's variant with four weight stages in flight
+  if (kernel == MOE_W4A16_KERNEL_PREFILL && block_m <= 128) p.tc_rows = 128;
   return run_gemm(p, kernel, num_tokens, s);
 }
 

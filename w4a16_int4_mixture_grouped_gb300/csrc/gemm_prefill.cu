@@ -50,43 +50,53 @@ __device__ __forceinline__ unsigned long long* pipe_stats_ptr() { return g_pipe_
 __device__ __forceinline__ unsigned long long* pipe_stats_ptr() { return nullptr; }
 #endif
 
-constexpr int kDequantWarps = 16;          // one 16-channel m-tile of the unit each per k-chunk
+constexpr int kDequantWarps = 16;          // the unit's 16 m-tiles of each k-chunk, split between groups
 constexpr int kIssuers = 2;                // MMA-issuing warps, one per 128-channel tile
 constexpr int kThreads = (4 + kDequantWarps) * 32;
-constexpr int kRows = kPrefillRows;        // 192: rows (MMA N) per block
 #ifndef MOE_W4A16_PREFILL_XSTAGES
 #define MOE_W4A16_PREFILL_XSTAGES 5
 #endif
 #ifndef MOE_W4A16_PREFILL_PSTAGES
 #define MOE_W4A16_PREFILL_PSTAGES 6
 #endif
-constexpr int kXStages = MOE_W4A16_PREFILL_XSTAGES;   // activation tiles (24 KB each)
-#ifndef MOE_W4A16_PREFILL_WSTAGES
-#define MOE_W4A16_PREFILL_WSTAGES 2
-#endif
-constexpr int kWStages = MOE_W4A16_PREFILL_WSTAGES;   // dequantised weight stages, in TMEM
-constexpr int kPStages = MOE_W4A16_PREFILL_PSTAGES;   // packed weight chunks (9 KB each)
-constexpr int kXBytes = kRows * 128;       // 24 KB: 192 rows x 64 k x bf16 (multiple of 1024)
 constexpr int kPBytes = 2 * kChunkBytes;   // 9 KB
-constexpr int kXOff = 0;
-constexpr int kPOff = kXOff + kXStages * kXBytes;
-constexpr int kBarOff = kPOff + kPStages * kPBytes;
-constexpr int kNumBars = 2 * kPStages + 2 * kXStages + 2 * kWStages + 3;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kPrefixOff = kMiscOff + 16;           // masked: int [E + 1] block prefix
 // TMEM (512 columns x 128 lanes x 32 bit): FP32 accumulators of the two 128-channel tiles at
-// columns [0, kRows) and [kRows, 2 kRows); dequantised BF16 weights, the MMA's A operand
-// (lane = channel, column c = k pair 2c, 2c+1), in kWStages stages of 2 tiles x 32 columns.
+// columns [0, ROWS) and [ROWS, 2 ROWS); dequantised BF16 weights, the MMA's A operand
+// (lane = channel, column c = k pair 2c, 2c+1), in the stages of 2 tiles x 32 columns that fit after them.
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = kRows;
-constexpr int kACol0 = 2 * kAccCols;                // 384
 constexpr int kAStageCols = 2 * (kChunkK / 2);      // 64
-static_assert(kACol0 + kWStages * kAStageCols <= kTmemCols, "TMEM budget");
-static_assert(kXBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
-__host__ __device__ constexpr int smem_bytes(int prefix_entries) {
-  return kPrefixOff + prefix_entries * 4 + 1024;  // + alignment slack
-}
+// Geometry of the variant whose row blocks hold up to ROWS routed rows (MMA N). With 192 rows the
+// accumulators leave TMEM room for two weight stages, dequantised by two groups of eight warps on
+// alternate k-chunks (each warp one tile's two m-tiles of its TMEM lane quarter); with 128 rows four
+// stages fit, and four groups of four warps take every fourth chunk (each warp both tiles' m-tiles
+// of its lane quarter), so four chunks are in flight instead of two -- what blocks of few rows, whose
+// MMAs are short, are paced by.
+template <int ROWS>
+struct Cfg {
+  static constexpr int kRows = ROWS;
+  static constexpr int kWStages = (kTmemCols - 2 * ROWS) / kAStageCols;   // 2 or 4
+  static constexpr int kGroups = kWStages;
+  static constexpr int kGroupWarps = kDequantWarps / kGroups;            // 8 or 4
+  static constexpr int kTilesPerWarp = kGroups / 2;                      // 1 or 2
+  static constexpr int kXStages = ROWS == 192 ? MOE_W4A16_PREFILL_XSTAGES : 6;   // activation tiles
+  static constexpr int kPStages = ROWS == 192 ? MOE_W4A16_PREFILL_PSTAGES : 8;   // packed weight chunks
+  static constexpr int kXBytes = ROWS * 128;      // ROWS rows x 64 k x bf16 (a multiple of 1024)
+  static constexpr int kXOff = 0;
+  static constexpr int kPOff = kXOff + kXStages * kXBytes;
+  static constexpr int kBarOff = kPOff + kPStages * kPBytes;
+  static constexpr int kNumBars = 2 * kPStages + 2 * kXStages + 2 * kWStages + 3;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kPrefixOff = kMiscOff + 16;   // masked: int [E + 1] block prefix
+  static constexpr int kAccCols = ROWS;
+  static constexpr int kACol0 = 2 * kAccCols;
+  static_assert(kACol0 + kWStages * kAStageCols <= kTmemCols, "TMEM budget");
+  static_assert(kXBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(kGroups == 2 || kGroups == 4, "two or four dequantisation groups");
+  static constexpr int smem_bytes(int prefix_entries) {
+    return kPrefixOff + prefix_entries * 4 + 1024;  // + alignment slack
+  }
+};
 
 // ---------------------------------------------------------------------------
 // tcgen05 wrappers
@@ -207,9 +217,13 @@ __device__ __forceinline__ int block_extent(const GemmParams& p, int blk, int e,
 }
 
 // DIAG: the diagnostic instantiation, whose waits take the launch's own limit (moe_w4a16_set_wait_limit_ns).
-template <bool DIAG>
+template <bool DIAG, int ROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_gemm_kernel(const GemmParams p, const __grid_constant__ XMaps xmaps) {
+  using C = Cfg<ROWS>;
+  constexpr int kRows = C::kRows, kWStages = C::kWStages, kXStages = C::kXStages, kPStages = C::kPStages;
+  constexpr int kXBytes = C::kXBytes, kXOff = C::kXOff, kPOff = C::kPOff, kBarOff = C::kBarOff;
+  constexpr int kMiscOff = C::kMiscOff, kPrefixOff = C::kPrefixOff, kAccCols = C::kAccCols, kACol0 = C::kACol0;
   // a split call without experts above the decode kernel's rows: nothing to do (before any
   // barrier or TMEM is set up)
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED && p.cblocks != nullptr && p.cblocks[0].x <= 0) return;
@@ -230,14 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(p_full + 8 * i, 1);
-      mbar_init(p_empty + 8 * i, kDequantWarps / 2);   // the chunk's dequantisation group
+      mbar_init(p_empty + 8 * i, C::kGroupWarps);   // the chunk's dequantisation group
     }
     for (int i = 0; i < kXStages; ++i) {
       mbar_init(x_full + 8 * i, 1);
       mbar_init(x_empty + 8 * i, kIssuers);
     }
     for (int i = 0; i < kWStages; ++i) {
-      mbar_init(w_full + 8 * i, kDequantWarps / 2);
+      mbar_init(w_full + 8 * i, C::kGroupWarps);
       mbar_init(w_empty + 8 * i, kIssuers);
     }
     mbar_init(acc_full, kIssuers);
@@ -434,8 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile = (dw >> 2) & 1;
     const int mj = dw >> 3;
     const int g = lane >> 2;
-    const int grp = dw >> 3;            // dequantisation group: even (0) or odd (1) k-chunks
-    const int dq_tile = (dw >> 2) & 1;  // tile whose lane quarter wq this warp dequantises
+    // dequantisation group (it takes the k-chunks gch with gch % kGroups == grp) and the first tile
+    // whose lane quarter wq this warp dequantises (its only one with two groups, tile 0 of two with four)
+    const int grp = dw / C::kGroupWarps;
+    const int dq_tile = C::kTilesPerWarp == 1 ? (dw >> 2) & 1 : 0;
     int ps = 0, ws = 0;
     uint32_t pph = 0, aph = 0;
     uint32_t gch = 0;   // k-chunks this CTA has dequantised
@@ -463,10 +479,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int blk = cur.blk, gp = cur.gp, e = cur.e, local = cur.local, ext = cur.ext;
       const int nr = (ext + 15) & ~15;
       for (int kc = 0; kc < p.KC; ++kc) {
-        // k-chunks alternate between the two groups of eight warps (half the barrier traffic of
-        // sixteen warps per chunk, and twice the independent work per warp); the other group's
-        // chunks only advance this warp's stage counters
-        if ((gch & 1u) != static_cast<uint32_t>(grp)) {
+        // k-chunks go round the groups (fewer barrier arrivals per chunk than sixteen warps, more
+        // independent work per warp, and one chunk in flight per group); the other groups' chunks
+        // only advance this warp's stage counters
+        if ((gch & static_cast<uint32_t>(C::kGroups - 1)) != static_cast<uint32_t>(grp)) {
           if (++ps == kPStages) {
             ps = 0;
             pph ^= 1u;
@@ -478,14 +494,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         pst.start();
         if (!warp_wait(p_full + 8 * ps, pph, abort_flag, p.err, wait_limit<DIAG>(p))) goto d_done;
         pst.stop(0);
-        const uint32_t pa = sbase + kPOff + ps * kPBytes + dq_tile * kChunkBytes;
-        uint4 wv[2];
-        uint2 sv[2];
+        constexpr int kT = C::kTilesPerWarp;
+        uint4 wv[kT][2];
+        uint2 sv[kT][2];
 #pragma unroll
-        for (int m2 = 0; m2 < 2; ++m2) {
-          const int mt = 2 * wq + m2;
-          wv[m2] = lds128(pa + (mt * 32 + lane) * 16);
-          sv[m2] = lds64(pa + kChunkWBytes + (mt * 8 + g) * 8);
+        for (int tt = 0; tt < kT; ++tt) {
+          const uint32_t pa = sbase + kPOff + ps * kPBytes + (dq_tile + tt) * kChunkBytes;
+#pragma unroll
+          for (int m2 = 0; m2 < 2; ++m2) {
+            const int mt = 2 * wq + m2;
+            wv[tt][m2] = lds128(pa + (mt * 32 + lane) * 16);
+            sv[tt][m2] = lds64(pa + kChunkWBytes + (mt * 8 + g) * 8);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(p_empty + 8 * ps);
@@ -499,27 +519,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(w_empty + 8 * ws, ((gch / kWStages) & 1u) ^ 1u, abort_flag, p.err, wait_limit<DIAG>(p))) goto d_done;
         pst.stop(1);
         pst.start();
-        // A operand of this tile: TMEM lanes = channels (this warp's quarter), columns = k pairs of
+        // A operand of a tile: TMEM lanes = channels (this warp's quarter), columns = k pairs of
         // the 64-k chunk; m-tile m2 at lanes 32 wq + 16 m2
-        const uint32_t at = tmem + kACol0 + ws * kAStageCols + dq_tile * (kAStageCols / 2) +
-                            (static_cast<uint32_t>(32 * wq) << 16);
 #pragma unroll
-        for (int m2 = 0; m2 < 2; ++m2) {
-          const uint32_t w4[4] = {wv[m2].x, wv[m2].y, wv[m2].z, wv[m2].w};
-          uint32_t sg[2], sg8[2];
-          scale_pairs(sv[m2], 0, sg[0], sg8[0]);
-          scale_pairs(sv[m2], 1, sg[1], sg8[1]);
-          uint32_t frag[16];
+        for (int tt = 0; tt < kT; ++tt) {
+          const uint32_t at = tmem + kACol0 + ws * kAStageCols + (dq_tile + tt) * (kAStageCols / 2) +
+                              (static_cast<uint32_t>(32 * wq) << 16);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            uint32_t a[4];
-            dequant_fu(w4[ks], sg[ks >> 1], sg8[ks >> 1], a);
-            frag[4 * ks + 0] = a[0];
-            frag[4 * ks + 1] = a[1];
-            frag[4 * ks + 2] = a[2];
-            frag[4 * ks + 3] = a[3];
+          for (int m2 = 0; m2 < 2; ++m2) {
+            const uint32_t w4[4] = {wv[tt][m2].x, wv[tt][m2].y, wv[tt][m2].z, wv[tt][m2].w};
+            uint32_t sg[2], sg8[2];
+            scale_pairs(sv[tt][m2], 0, sg[0], sg8[0]);
+            scale_pairs(sv[tt][m2], 1, sg[1], sg8[1]);
+            uint32_t frag[16];
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              uint32_t a[4];
+              dequant_fu(w4[ks], sg[ks >> 1], sg8[ks >> 1], a);
+              frag[4 * ks + 0] = a[0];
+              frag[4 * ks + 1] = a[1];
+              frag[4 * ks + 2] = a[2];
+              frag[4 * ks + 3] = a[3];
+            }
+            tmem_st_16x128b_x8(at + (static_cast<uint32_t>(16 * m2) << 16), frag);
           }
-          tmem_st_16x128b_x8(at + (static_cast<uint32_t>(16 * m2) << 16), frag);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -640,28 +663,40 @@ cudaError_t launch_prefill_gemm(const GemmParams& p, int device, cudaStream_t st
   }
   const DeviceInfo& di = device_info(device);
   const int prefix_entries = p.layout == MOE_W4A16_LAYOUT_MASKED ? p.num_experts + 1 : 0;
-  const int smem = smem_bytes(prefix_entries);
   const bool diag = p.wait_ns != kWaitLimitNs;
-  static bool attr_set[2][64] = {{false}};
-  if (device >= 0 && device < 64 && !attr_set[diag][device]) {
-    cudaError_t e = cudaFuncSetAttribute(diag ? prefill_gemm_kernel<true> : prefill_gemm_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
+  // the 128-row variant for calls whose blocks hold at most 128 rows and that ask for it (tc_rows)
+  const bool small = p.tc_rows == 128 && p.layout == MOE_W4A16_LAYOUT_INDEXED &&
+                     (p.cblocks != nullptr || p.block_m <= 128);
+  const int rows = small ? 128 : 192;
+  const int smem = small ? Cfg<128>::smem_bytes(prefix_entries) : Cfg<192>::smem_bytes(prefix_entries);
+  static bool attr_set[2][2][64] = {{{false}}};
+  if (device >= 0 && device < 64 && !attr_set[small][diag][device]) {
+    const void* fn = small ? (diag ? reinterpret_cast<const void*>(prefill_gemm_kernel<true, 128>)
+                                   : reinterpret_cast<const void*>(prefill_gemm_kernel<false, 128>))
+                           : (diag ? reinterpret_cast<const void*>(prefill_gemm_kernel<true, 192>)
+                                   : reinterpret_cast<const void*>(prefill_gemm_kernel<false, 192>));
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         small ? Cfg<128>::smem_bytes(MOE_W4A16_MAX_EXPERTS + 1)
+                                               : Cfg<192>::smem_bytes(MOE_W4A16_MAX_EXPERTS + 1));
     if (e != cudaSuccess) return e;
-    attr_set[diag][device] = true;
+    attr_set[small][diag][device] = true;
   }
   int64_t max_blocks;
   if (p.layout == MOE_W4A16_LAYOUT_INDEXED) max_blocks = p.cblocks != nullptr ? p.cb_cap : p.sorted_cap / p.block_m;
   else if (p.layout == MOE_W4A16_LAYOUT_CONTIGUOUS) max_blocks = p.m_pad / kContigSeg;
-  else max_blocks = static_cast<int64_t>(p.num_experts) * ((p.max_m + kRows - 1) / kRows);
+  else max_blocks = static_cast<int64_t>(p.num_experts) * ((p.max_m + rows - 1) / rows);
   int64_t units = max_blocks * p.NG;
   int64_t grid = di.sm_count;
   if (units < grid) grid = units;
   if (grid < 1) grid = 1;
-  if (diag)
-    prefill_gemm_kernel<true><<<static_cast<int>(grid), kThreads, smem, stream>>>(p, xmaps);
-  else
-    prefill_gemm_kernel<false><<<static_cast<int>(grid), kThreads, smem, stream>>>(p, xmaps);
+  const dim3 g(static_cast<unsigned>(grid));
+  if (small) {
+    if (diag) prefill_gemm_kernel<true, 128><<<g, kThreads, smem, stream>>>(p, xmaps);
+    else prefill_gemm_kernel<false, 128><<<g, kThreads, smem, stream>>>(p, xmaps);
+  } else {
+    if (diag) prefill_gemm_kernel<true, 192><<<g, kThreads, smem, stream>>>(p, xmaps);
+    else prefill_gemm_kernel<false, 192><<<g, kThreads, smem, stream>>>(p, xmaps);
+  }
   note_launch();
   if (grid_out) *grid_out = static_cast<int>(grid);
   return cudaGetLastError();

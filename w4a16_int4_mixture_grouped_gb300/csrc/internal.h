@@ -74,6 +74,8 @@ struct GemmParams {
   const int4* cblocks;       // tcgen05 kernel: table of row blocks {first row / slot, expert, rows, 0}: contiguous
                              // merged blocks, or the indexed split's blocks of experts above kSplitRows rows
   int cb_cap;                // indexed split: entries the table holds
+  int tc_rows;               // tcgen05 kernel: 128 selects its 128-row variant (indexed blocks of at most 128
+                             // rows, or a split table cut into 128-row blocks); otherwise 192 rows
   const int32_t* hot;        // indexed split, decode kernel: experts (flag 1) the tcgen05 kernel takes
 
   // masked
@@ -122,11 +124,12 @@ cudaError_t launch_gather_sorted(const uint16_t* src, int64_t src_rows, int K, c
 // Row blocks of a contiguous layout for the tcgen05 kernel (see layout.cu): table[0].x = count,
 // table[1 + b] = {first row, expert, rows, 0}; at most kMaxContigSegs segments (else an error).
 cudaError_t launch_contig_blocks(const int32_t* m_indices, int m_pad, int4* table, cudaStream_t stream);
+// block_rows: rows per tcgen05 table block (the split uses kSplitTcRows).
 cudaError_t launch_split_table(const int32_t* sorted_ids, const int32_t* expert_ids, const int32_t* num_post_padded,
-                               int64_t sorted_cap, int block_m, int R, int E, int cap, int4* table, int32_t* hot,
-                               int* err, cudaStream_t stream);
+                               int64_t sorted_cap, int block_m, int block_rows, int R, int E, int cap, int4* table,
+                               int32_t* hot, int* err, cudaStream_t stream);
 cudaError_t launch_gather_table(const uint16_t* src, int64_t src_rows, int K, const int32_t* sorted_ids,
-                                const int4* table, int cap, int R, int row_div, uint16_t* dst, int* err,
+                                const int4* table, int cap, int block_rows, int R, int row_div, uint16_t* dst, int* err,
                                 cudaStream_t stream);
 
 // out[t, :] = bf16(sum_j w[t, j] * y[t*top_k + j, :]), j ascending, FP32 sums.
@@ -166,9 +169,14 @@ constexpr int kDecodeRowsSmall = 16;   // decode blocks this small run three CTA
 constexpr int kPrefillRows = MOE_W4A16_PREFILL_ROWS;   // two 128-channel accumulators of 192 columns + weight stages fill TMEM
 constexpr int kContigSeg = 128;
 // Indexed split (MOE_W4A16_FLAG_SPLIT): experts with more than kSplitRows routed rows run on the
-// tcgen05 kernel in blocks of up to kPrefillRows rows; the plan proposes it for kSplitMinTokE <= tok_e <
-// kSplitMaxTokE.
+// tcgen05 kernel in blocks of up to kSplitTcRows rows; the plan proposes it for kSplitMinTokE <= tok_e <
+// kSplitMaxTokE. (128-row blocks on the kernel's 128-row variant: 4096 tokens uniform -1.8%, Zipf +10%,
+// a hot expert's units cost about the same whatever their rows.)
 constexpr int kSplitRows = 32;
+#ifndef MOE_W4A16_SPLIT_TC_ROWS
+#define MOE_W4A16_SPLIT_TC_ROWS 192
+#endif
+constexpr int kSplitTcRows = MOE_W4A16_SPLIT_TC_ROWS;
 constexpr int kSplitMinTokE = 8;
 #ifndef MOE_W4A16_SPLIT_MAX_TOKE
 #define MOE_W4A16_SPLIT_MAX_TOKE 128   // 4096 tokens at top-8 over 384 experts (86 rows/expert) split too:
@@ -176,7 +184,7 @@ constexpr int kSplitMinTokE = 8;
 #endif
 constexpr int kSplitMaxTokE = MOE_W4A16_SPLIT_MAX_TOKE;
 // Entries of the split's block table for R routed rows: every hot expert has more than kSplitRows rows.
-constexpr int64_t split_table_cap(int64_t R) { return R / kPrefillRows + R / (kSplitRows + 1) + 1; }
+constexpr int64_t split_table_cap(int64_t R) { return R / kSplitTcRows + R / (kSplitRows + 1) + 1; }
 constexpr int kMaxContigSegs = 2048;   // merged contiguous blocks: at most 2048 segments (262144 rows)
 // Routed calls (moe_w4a16_indexed_routed): the block layout a CTA keeps in shared memory, in 32-bit
 // words: a 32-bit count per expert, then 16-bit first rows and first blocks per expert (E + 1 each)

@@ -387,13 +387,13 @@ cudaError_t launch_contiguous_layout(const int32_t* sorted_ids, const int32_t* e
 
 // The split of an indexed call (align with block_m <= 32): the routed rows of each expert,
 // counted from its blocks; experts with more than kSplitRows rows are flagged for the
-// tcgen05 kernel and their slots cut into table blocks of up to kPrefillRows rows, in
+// tcgen05 kernel and their slots cut into table blocks of up to block_rows rows, in
 // expert order. table[0].x = block count; table[1 + b] = {first slot, expert, rows, 0}.
 // One CTA of 1024 threads (one expert per thread in the scan).
 __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __restrict__ sorted_ids,
                                                              const int32_t* __restrict__ expert_ids,
                                                              const int32_t* __restrict__ npp, int64_t sorted_cap,
-                                                             int block_m, int R, int E, int cap,
+                                                             int block_m, int block_rows, int R, int E, int cap,
                                                              int4* __restrict__ table, int32_t* __restrict__ hot,
                                                              int* err) {
   __shared__ int first[MOE_W4A16_MAX_EXPERTS];      // an expert's first and last block
@@ -443,15 +443,15 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
   const int e = t;
   const int c = e < E && last[e] >= first[e] ? (last[e] - first[e]) * block_m + last_rows[e] : 0;
   const bool is_hot = c > kSplitRows;
-  // a hot expert's rows past its last full kPrefillRows block, when they are no more than a
+  // a hot expert's rows past its last full block_rows block, when they are no more than a
   // decode block's and start on a block boundary, go to the decode side too: a tcgen05 unit
   // costs the same whatever its rows, so a few-row remainder block is better streamed there
-  const int full = c / kPrefillRows, rem = c - full * kPrefillRows;
-  const bool rem_cold = is_hot && full > 0 && rem > 0 && rem <= kSplitRows && kPrefillRows % block_m == 0;
-  const int nbk = is_hot ? (rem_cold ? full : (c + kPrefillRows - 1) / kPrefillRows) : 0;
+  const int full = c / block_rows, rem = c - full * block_rows;
+  const bool rem_cold = is_hot && full > 0 && rem > 0 && rem <= kSplitRows && block_rows % block_m == 0;
+  const int nbk = is_hot ? (rem_cold ? full : (c + block_rows - 1) / block_rows) : 0;
   if (e < E) {
     hot[e] = is_hot ? (rem_cold ? 2 : 1) : 0;
-    cold_from[e] = !is_hot ? 0 : (rem_cold ? full * (kPrefillRows / block_m) : 0x7fffffff);
+    cold_from[e] = !is_hot ? 0 : (rem_cold ? full * (block_rows / block_m) : 0x7fffffff);
   }
   int incl = nbk;
 #pragma unroll
@@ -475,8 +475,8 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
   const int slot0 = first[e < E ? e : 0] * block_m;
   for (int j = 0; j < nbk; ++j) {
     if (base + j >= cap) break;
-    const int rows = c - j * kPrefillRows < kPrefillRows ? c - j * kPrefillRows : kPrefillRows;
-    table[1 + base + j] = make_int4(slot0 + j * kPrefillRows, e, rows, 0);
+    const int rows = c - j * block_rows < block_rows ? c - j * block_rows : block_rows;
+    table[1 + base + j] = make_int4(slot0 + j * block_rows, e, rows, 0);
   }
   if (t == 0) {
     const int total = wsum[31];
@@ -527,10 +527,10 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
 __global__ void __launch_bounds__(256) gather_table_kernel(const uint4* __restrict__ src, int64_t src_rows, int KV,
                                                             const int32_t* __restrict__ sorted_ids,
                                                             const int4* __restrict__ table, int cap, int R,
-                                                            int row_div, uint4* __restrict__ dst, int* err) {
-  constexpr int kParts = kPrefillRows / 8;
-  const int b = blockIdx.x / kParts;
-  const int i = (blockIdx.x % kParts) * 8 + (threadIdx.x >> 5);
+                                                            int row_div, int parts, uint4* __restrict__ dst,
+                                                            int* err) {
+  const int b = blockIdx.x / parts;
+  const int i = (blockIdx.x % parts) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   int nb = table[0].x;
   nb = nb < 0 ? 0 : (nb > cap ? cap : nb);
@@ -549,23 +549,24 @@ __global__ void __launch_bounds__(256) gather_table_kernel(const uint4* __restri
 }
 
 cudaError_t launch_gather_table(const uint16_t* src, int64_t src_rows, int K, const int32_t* sorted_ids,
-                                const int4* table, int cap, int R, int row_div, uint16_t* dst, int* err,
+                                const int4* table, int cap, int block_rows, int R, int row_div, uint16_t* dst, int* err,
                                 cudaStream_t stream) {
-  const int64_t blocks = static_cast<int64_t>(cap) * (kPrefillRows / 8);
+  if (block_rows < 8 || block_rows % 8 != 0) return cudaErrorInvalidValue;
+  const int64_t blocks = static_cast<int64_t>(cap) * (block_rows / 8);
   if (blocks < 1 || blocks > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
   gather_table_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(src), src_rows, K / 8, sorted_ids, table, cap, R, row_div,
+      reinterpret_cast<const uint4*>(src), src_rows, K / 8, sorted_ids, table, cap, R, row_div, block_rows / 8,
       reinterpret_cast<uint4*>(dst), err);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_split_table(const int32_t* sorted_ids, const int32_t* expert_ids, const int32_t* num_post_padded,
-                               int64_t sorted_cap, int block_m, int R, int E, int cap, int4* table, int32_t* hot,
-                               int* err, cudaStream_t stream) {
-  if (E < 1 || E > MOE_W4A16_MAX_EXPERTS || block_m < 1) return cudaErrorInvalidValue;
-  split_table_kernel<<<1, 1024, 0, stream>>>(sorted_ids, expert_ids, num_post_padded, sorted_cap, block_m, R, E, cap,
-                                             table, hot, err);
+                               int64_t sorted_cap, int block_m, int block_rows, int R, int E, int cap, int4* table,
+                               int32_t* hot, int* err, cudaStream_t stream) {
+  if (E < 1 || E > MOE_W4A16_MAX_EXPERTS || block_m < 1 || block_rows <= kSplitRows) return cudaErrorInvalidValue;
+  split_table_kernel<<<1, 1024, 0, stream>>>(sorted_ids, expert_ids, num_post_padded, sorted_cap, block_m, block_rows,
+                                             R, E, cap, table, hot, err);
   note_launch();
   return cudaGetLastError();
 }
