@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "rows.cuh"
 
 namespace moe {
 
@@ -42,7 +43,8 @@ __device__ __forceinline__ int warp_inclusive_sum(int v, int lane) {
 //  C. per-expert start offsets (padded to block_m, or e*max_m when masked) by a
 //     block-wide scan, one expert per thread;
 //  D. each warp walks its rows in order, ranking equal experts within a
-//     32-row step with match.any, so rows land in ascending f per expert;
+//     32-row step by a mask of the lanes holding the same expert (one ballot
+//     per bit of the expert id), so rows land in ascending f per expert;
 //  E. padding sentinels and the expert of every row block, experts spread
 //     over the cluster's warps.
 // No global scratch: the cross-CTA exchange stays on chip. A CTA signals that
@@ -70,6 +72,7 @@ __global__ void __cluster_dims__(kAlignCtas, 1, 1) __launch_bounds__(kAlignWarps
   const int wsteps = (steps + kAlignWarps - 1) / kAlignWarps;
   const int nw = wsteps > 0 ? (steps + wsteps - 1) / wsteps : 0;   // warps holding rows
   const int beg = min(cend, cbeg + warp * wsteps * 32), end = min(cend, beg + wsteps * 32);
+  const int nbits = 32 - __clz(E + 31);   // expert ids and the per-lane stand-ins E + lane of invalid ones
   for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   for (int b0 = beg; b0 < end; b0 += 32 * kAlignBatch) {
@@ -146,7 +149,7 @@ __global__ void __cluster_dims__(kAlignCtas, 1, 1) __launch_bounds__(kAlignWarps
       const int i = b0 + 32 * j + lane;
       const int x = ev[j];
       const bool valid = i < end && x >= 0 && x < E;
-      const unsigned peers = __match_any_sync(0xffffffffu, valid ? x : E + lane);
+      const unsigned peers = equal_lanes(valid ? x : E + lane, nbits);
       const int rk = __popc(peers & ((1u << lane) - 1u));
       int off = 0;
       if (valid) off = before[x] + hist[warp * E + x] + rk;
