@@ -112,7 +112,7 @@ enum {
 #define MOE_W4A16_VERSION 1u
 #define MOE_W4A16_MAX_EXPERTS 1024
 #define MOE_W4A16_WS_HEADER_BYTES 256
-#define MOE_W4A16_STATIC_SCRATCH_BYTES (48u << 20) /* scratch of moe_w4a16_indexed_noalloc */
+#define MOE_W4A16_STATIC_SCRATCH_BYTES (64u << 20) /* scratch of moe_w4a16_indexed_noalloc */
 #define MOE_W4A16_WAIT_LIMIT_NS 2000000000ull      /* default limit of a device pipeline wait */
 #define MOE_W4A16_ROUTED_MAX_ROWS 4096             /* routed rows of a moe_w4a16_indexed_routed call */
 
@@ -375,7 +375,7 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad
  * It computes exactly what moe_w4a16_indexed computes for block_m 1..32, with
  * the same arguments except the workspace, and takes its scratch (device error
  * word, combine counters, combine staging rows, decode partial tiles) from one statically reserved
- * device array of MOE_W4A16_STATIC_SCRATCH_BYTES (48 MiB) per device.
+ * device array of MOE_W4A16_STATIC_SCRATCH_BYTES (64 MiB) per device.
  *   block_m    1..32 (decode kernel only), else INVALID_ARG
  *   flags      as for moe_w4a16_indexed, except MOE_W4A16_FLAG_SPLIT (INVALID_ARG: it
  *              would also run the tcgen05 kernel)
@@ -383,8 +383,9 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_contiguous(const uint16_t* a, int m_pad
  *              whose first int32 is this call's device error word (read it with
  *              moe_w4a16_get_device_error). Owned by the library: never free it.
  * A call whose moe_w4a16_workspace_size exceeds MOE_W4A16_STATIC_SCRATCH_BYTES
- * (10.0 MB of decode partial tiles at block_m <= 16, 19.9 MB above; with
- * COMBINE also 2*num_tokens*top_k*n bytes of staging) returns
+ * (19.9 MB of decode partial tiles at block_m <= 16, 39.9 MB above; with
+ * COMBINE also 2*num_tokens*top_k*n bytes of staging: at top-8 and n = 7168
+ * up to 408 tokens at block_m <= 16, 235 above) returns
  * MOE_W4A16_ERR_SCRATCH_LIMIT before any CUDA call. No cudaMalloc, cudaFree or
  * allocating library routine is called.
  * Set-up: the first call on a device, with that device current, resolves the

@@ -169,14 +169,14 @@ def test_gemm_host_checks_reject_before_launch(lib):
 
 
 def test_noalloc_rejects_before_any_cuda_call(lib):
-    """The static-scratch entry point refuses calls whose scratch exceeds 48 MiB, prefill block sizes and the split."""
+    """The static-scratch entry point refuses calls whose scratch exceeds 64 MiB, prefill block sizes and the split."""
     d = _desc(e=4, n=1024, k=64)
 
     def call(t, k, block_m, flags, desc=d):
         return lib.moe_w4a16_indexed_noalloc(FAKE, t * k, 64, ctypes.byref(desc) if desc else None, FAKE, FAKE, FAKE, FAKE, t, k, block_m, FAKE,
                                              ctypes.c_uint32(flags), FAKE, None, None)
 
-    assert call(3200, 8, 16, 2 | 4) == 9              # counters + 3200*8*1024*2 B + partial tiles > 48 MiB
+    assert call(3200, 8, 16, 2 | 4) == 9              # counters + 3200*8*1024*2 B + partial tiles > 64 MiB
     assert call(8, 8, 64, 0) == 1                     # block_m above 32 runs the prefill kernel: refused
     assert call(8, 8, 0, 0) == 1
     assert call(8, 8, 16, 0, desc=None) == 1
@@ -209,3 +209,29 @@ def test_routed_rejects_before_any_cuda_call(lib):
     assert call(1025, 4, 16) == 2                     # 4100 routed rows > 4096
     assert call(8, 2, 16, ids=None) == 1              # no ids
     assert call(8, 2, 16, a_rows=9) == 1              # A rows must be the token count
+
+
+def test_binding_constants_match_the_header(lib):
+    """Every enum value and size the binding restates equals the header's: a mismatch would pass the wrong flag or
+    size through the C ABI without any error."""
+    import w4a16_int4_mixture_grouped_gb300 as M
+    text = open(HEADER).read()
+    vals = {}
+    for name, v in re.findall(r"\b(MOE_W4A16_[A-Z0-9_]+)\s*=\s*(\d+)u?\s*[,/\n]", text):
+        vals[name] = int(v)
+    for name, expr in re.findall(r"#define (MOE_W4A16_[A-Z0-9_]+) \(?([0-9a-fx]+u?(?: << \d+)?)\)?", text):
+        vals[name] = eval(expr.replace("ull", "").replace("u", ""))
+    expect = {
+        "LAYOUT_INDEXED": M.LAYOUT_INDEXED, "LAYOUT_CONTIGUOUS": M.LAYOUT_CONTIGUOUS, "LAYOUT_MASKED": M.LAYOUT_MASKED,
+        "MODE_PLAIN": M.MODE_PLAIN, "MODE_GATE_UP": M.MODE_GATE_UP,
+        "FLAG_SWIGLU": M.FLAG_SWIGLU, "FLAG_COMBINE": M.FLAG_COMBINE, "FLAG_A_PER_ROW": M.FLAG_A_PER_ROW,
+        "FLAG_A_SORTED": M.FLAG_A_SORTED, "FLAG_OUT_SORTED": M.FLAG_OUT_SORTED, "FLAG_SPLIT": M.FLAG_SPLIT,
+        "KERNEL_AUTO": M.KERNEL_AUTO, "KERNEL_DECODE": M.KERNEL_DECODE, "KERNEL_PREFILL": M.KERNEL_PREFILL,
+        "KERNEL_SPLIT": M.KERNEL_SPLIT, "WS_HEADER_BYTES": M.WS_HEADER_BYTES,
+        "STATIC_SCRATCH_BYTES": M.STATIC_SCRATCH_BYTES, "WAIT_LIMIT_NS": M.WAIT_LIMIT_NS,
+        "ROUTED_MAX_ROWS": M.ROUTED_MAX_ROWS,
+    }
+    for name, v in expect.items():
+        assert vals["MOE_W4A16_" + name] == v, name
+    for code, name in M.STATUS_NAMES.items():
+        assert vals["MOE_W4A16_" + name] == code, name

@@ -107,7 +107,7 @@ def test_noalloc_rejects_oversize_and_prefill_block():
     e, kd, n = 4, 64, 1024
     qw, sc = random_weights(rng, e, n, kd)
     pw = prepare_dev(qw, sc, 1, DEV)
-    t, k = 3200, 8                      # combine staging 3200*8*1024*2 B + partial tiles > 48 MiB
+    t, k = 3200, 8                      # combine staging 3200*8*1024*2 B + partial tiles > 64 MiB
     need = M.workspace_size(M.LAYOUT_INDEXED, t, k, e, n, kd, 16, M.FLAG_COMBINE | M.FLAG_A_PER_ROW)
     assert need > M.STATIC_SCRATCH_BYTES
     dummy_i = torch.zeros(16, dtype=torch.int32, device=DEV)

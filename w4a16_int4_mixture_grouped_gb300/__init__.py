@@ -25,7 +25,7 @@ MODE_PLAIN, MODE_GATE_UP = 1, 2
 FLAG_SWIGLU, FLAG_COMBINE, FLAG_A_PER_ROW, FLAG_A_SORTED, FLAG_OUT_SORTED, FLAG_SPLIT = 1, 2, 4, 8, 16, 32
 KERNEL_AUTO, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_SPLIT = 0, 1, 2, 3
 WS_HEADER_BYTES = 256
-STATIC_SCRATCH_BYTES = 48 << 20   # scratch array of indexed_noalloc, per device
+STATIC_SCRATCH_BYTES = 64 << 20   # scratch array of indexed_noalloc, per device
 
 STATUS_NAMES = {
     0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_MODE_MISMATCH", 4: "ERR_WORKSPACE",

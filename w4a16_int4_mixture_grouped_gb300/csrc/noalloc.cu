@@ -38,8 +38,9 @@
 namespace moe {
 namespace {
 
-// 48 MiB: the decode partial tiles of 32-row blocks (19.9 MB) plus the combine
-// counters and rows of 263 tokens x top-8 x 7168 channels; every call without COMBINE fits.
+// 64 MiB: the decode partial tiles of 32-row blocks (39.9 MB) plus the combine
+// counters and rows of 235 tokens x top-8 x 7168 channels (408 tokens with 16-row
+// blocks); every call without COMBINE fits.
 constexpr size_t kStaticScratchBytes = MOE_W4A16_STATIC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
