@@ -282,16 +282,18 @@ class OurArm:
             # decode-family indexed calls take the router's ids straight: one launch per call (each CTA
             # builds the block layout itself) instead of align + GEMM
             self.routed = (routed and layout == "indexed" and self.kernel_family == "decode" and r <= M.ROUTED_MAX_ROWS)
+            written_rows = out_rows   # output rows the GEMM writes (a masked call writes only the valid ones)
             if layout == "masked":
                 self.max_m = wl.max_m
                 self.expected_m = max(1, int(self.counts[self.counts > 0].mean())) if self.e_active else 1
                 self.a3 = torch.empty((e, self.max_m, kd), dtype=torch.bfloat16, device=dev)
                 out_rows = e * self.max_m       # flat masked output
                 self.out = torch.empty((out_rows, n), dtype=torch.bfloat16, device=dev)
+                a_rows = r                      # the GEMM reads each routed row's own copy in the 3-D input
             self.dominant_name = ("gate_up" if wl.stage == "gate_up" else "down+combine") + " GEMM"
             self.dom_flops = 2.0 * r * kd * n
             self.dom_bytes = (self.e_active * CHUNK_BYTES_PER_WEIGHT * kd * n + a_rows * kd * 2
-                              + out_rows * n * 2 + (r * n * 4 if self.flags & M.FLAG_COMBINE else 0))
+                              + written_rows * n * 2 + (r * n * 4 if self.flags & M.FLAG_COMBINE else 0))
             self.flops = self.dom_flops
             self.weight_bytes = self.e_active * CHUNK_BYTES_PER_WEIGHT * kd * n
             self.h2d = self.a_np.nbytes + ids.nbytes + (wts.nbytes if self.flags else 0)

@@ -105,7 +105,8 @@ enum {
   MOE_W4A16_KERNEL_AUTO = 0,
   MOE_W4A16_KERNEL_DECODE = 1, /* warp-level MMA, dequantised weights as the MMA M operand, <= 32 rows/block */
   MOE_W4A16_KERNEL_PREFILL = 2, /* tcgen05 MMA with TMEM accumulators, <= 256 rows/block */
-  MOE_W4A16_KERNEL_SPLIT = 3    /* indexed calls: both, split per expert (MOE_W4A16_FLAG_SPLIT, block_m 32) */
+  MOE_W4A16_KERNEL_SPLIT = 3    /* both, split per expert: indexed calls with MOE_W4A16_FLAG_SPLIT (block_m 32);
+                                   masked calls by themselves */
 };
 
 #define MOE_W4A16_MAGIC 0x34413457u /* "W4A4" little-endian tag */
@@ -251,14 +252,19 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_gather_sorted(const uint16_t* src, int 
 /* Chooses the kernel family and block_m from the routed rows per expert:
  * tok_e = T*top_k/E (indexed), m_pad/E (contiguous) or expected_m (masked,
  * a positive count used only to choose the launch; results never depend on
- * it). The environment variable MOE_W4A16_FORCE_KERNEL=decode|prefill
- * overrides the family (read on every call, part of the memo key). Indexed
+ * it). The environment variable MOE_W4A16_FORCE_KERNEL=decode|prefill|split
+ * overrides the family (read on every call, part of the memo key; split is
+ * prefill for contiguous calls). Indexed
  * block_m: 16 for the decode family at tok_e <= 4, 32 for the rest of the
  * decode family, 192 for the prefill family. Indexed calls with
  * 8 <= tok_e < 128 (without a forced family) get MOE_W4A16_KERNEL_SPLIT with
  * block_m 32: under skewed routing such calls mix experts of a few rows and
  * experts of hundreds, and each family serves its own (the caller passes
  * MOE_W4A16_FLAG_SPLIT; a call that also combines uses the decode family).
+ * Masked calls with 24 <= expected_m < 128 get MOE_W4A16_KERNEL_SPLIT and
+ * moe_w4a16_masked runs it itself: experts with masked_m <= 32 on the decode
+ * kernel, the others on the tcgen05 kernel, each reading the experts' rows in
+ * place (a combining call stays on the tcgen05 family).
  * `plan` is host. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_experts, int n, int k, int expected_m,
                                 moe_w4a16_schedule* plan);
@@ -407,7 +413,8 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_indexed_noalloc(const uint16_t* a, int 
 /* Masked layout (the Chord page, section "grouped operator entry points":
  * expected_m is a positive count used only to choose the launch, masked_m
  * holds the valid rows per expert, and the output is flat even though the
- * input is 3-D; rows past masked_m[e] are not written).
+ * input is 3-D; rows past masked_m[e] are not written). With 24 <= expected_m
+ * < 128 the call is split per expert (see moe_w4a16_plan): two launches.
  *   a3         bf16 [E, max_m, k]
  *   masked_m   int32 [E]; a count above max_m records MOE_W4A16_ERR_CAPACITY
  *   row_ids    int32 [E*max_m]: flat id of each row (COMBINE only, else may be NULL)

@@ -322,12 +322,12 @@ def test_mode_mismatch_fails_before_launch():
 
 @pytest.mark.parametrize("tokens,kernel,block_m,masked_kernel",
                          [(16, 1, 16, 1), (128, 1, 16, 1), (192, 1, 16, 1), (256, 1, 32, 1), (512, 3, 32, 1),
-                          (1536, 3, 32, 2), (3072, 3, 32, 2), (6096, 3, 32, 2), (6144, 2, 192, 2),
-                          (8192, 2, 192, 2)])
+                          (1024, 3, 32, 1), (1152, 3, 32, 3), (1536, 3, 32, 3), (3072, 3, 32, 3), (6096, 3, 32, 3),
+                          (6144, 2, 192, 2), (8192, 2, 192, 2)])
 def test_plan_picks_family_and_block_from_rows_per_expert(tokens, kernel, block_m, masked_kernel):
     """tok_e = T*top_k/E (384 experts, top-8): decode 16-row blocks up to 4 rows per expert, decode 32-row blocks
-    below 8, the split per expert (indexed) from 8 to 127, the tcgen05 family from 128 on; masked calls switch
-    from the decode to the tcgen05 family at 24 rows per expert."""
+    below 8, the split per expert (indexed) from 8 to 127, the tcgen05 family from 128 on; masked calls stay on the
+    decode family below 24 rows per expert and split per expert from 24 to 127."""
     s = M.plan(M.LAYOUT_INDEXED, tokens, 8, 384, 4096, 7168)
     assert (s.kernel, s.block_m) == (kernel, block_m)
     assert s.tok_e == -(-tokens * 8 // 384)
@@ -363,6 +363,38 @@ def test_cut_units_match_the_oracle(e, t, k, kd, flags, regime):
         assert_close(runs[0], y, f"cut units e={e} t={t}")
     for r in runs[1:]:
         assert np.array_equal(r, runs[0])
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_masked_split_matches_oracle(flags):
+    """expected_m in 24..127: the masked call splits per expert, experts with at most 32 rows on the decode kernel
+    and the others on the tcgen05 kernel (two launches over the same 3-D input, each expert's rows read in place);
+    counts around 32 and the 192-row block edges, an expert without rows, NaN past each count (never read); two
+    calls are bit-identical."""
+    rng = np.random.default_rng(870 + flags)
+    counts = [0, 1, 31, 32, 33, 64, 191, 192, 193, 7, 250]
+    e, kd, n, max_m = len(counts), 256, 512, 256
+    ids = ids_from_counts(rng, counts)
+    t = ids.shape[0]
+    a = random_acts(rng, t, kd)
+    qw, sc = random_weights(rng, e, n, kd)
+    masked_m, mrows = O.masked_layout(ids, e, max_m)
+    a3 = O.gather_rows(a, mrows.reshape(-1), 1).reshape(e, max_m, kd)
+    for ex in range(e):
+        a3[ex, masked_m[ex]:] = 0x7FC0
+    pw = prepare_dev(qw, sc, 2 if flags else 1, DEV)
+    ws = M.workspace(M.LAYOUT_MASKED, t, 1, e, n, kd, 0, 0, DEV)
+    assert M.plan(M.LAYOUT_MASKED, t, 1, e, n, kd, expected_m=40).kernel == M.KERNEL_SPLIT
+    before = M.launch_count()
+    outs = [dev_to_bits(M.masked(bits_to_dev(a3, DEV), i32_to_dev(masked_m, DEV), 40, pw, ws, flags=flags))
+            for _ in range(2)]
+    assert M.launch_count() - before == 4   # decode + tcgen05 per call
+    assert M.get_device_error(ws) == 0
+    y = O.indexed_gemm(a, ids, lambda x: (qw[x], sc[x]), n)
+    ref = O.swiglu(y) if flags else y
+    valid = mrows.reshape(-1) >= 0
+    assert_close(outs[0][valid], ref[mrows.reshape(-1)[valid]], f"masked split flags={flags}")
+    assert np.array_equal(outs[0][valid], outs[1][valid])
 
 
 SPLIT_COUNTS = [1, 5, 31, 32, 33, 0, 64, 191, 192, 193, 400, 2]

@@ -71,6 +71,7 @@ static int forced_kernel() {
   if (v == nullptr) return 0;
   if (std::strcmp(v, "decode") == 0) return static_cast<int>(MOE_W4A16_KERNEL_DECODE);
   if (std::strcmp(v, "prefill") == 0) return static_cast<int>(MOE_W4A16_KERNEL_PREFILL);
+  if (std::strcmp(v, "split") == 0) return static_cast<int>(MOE_W4A16_KERNEL_SPLIT);
   return 0;
 }
 
@@ -395,10 +396,16 @@ moe_w4a16_status moe_w4a16_plan(int layout, int num_tokens, int top_k, int num_e
   pl.tok_e = static_cast<int32_t>(tok_e > (1 << 30) ? (1 << 30) : tok_e);
   pl.kernel = tok_e < kDecodeMaxTokE ? MOE_W4A16_KERNEL_DECODE : MOE_W4A16_KERNEL_PREFILL;
   // indexed calls between the regimes: the family is chosen per expert (a measured 12-21% on
-  // Zipf-skewed routing at 512 and 1536 tokens, the same within 2% under uniform routing)
+  // Zipf-skewed routing at 512 and 1536 tokens, the same within 2% under uniform routing); masked
+  // calls from the per-call switch on (below it their decode launch would be followed by a tcgen05
+  // launch with nothing to do: a masked budget gives no cold-only guarantee)
   if (layout == MOE_W4A16_LAYOUT_INDEXED && tok_e >= kSplitMinTokE && tok_e < kSplitMaxTokE)
     pl.kernel = MOE_W4A16_KERNEL_SPLIT;
+  if (layout == MOE_W4A16_LAYOUT_MASKED && tok_e >= kDecodeMaxTokE && tok_e < kSplitMaxTokE)
+    pl.kernel = MOE_W4A16_KERNEL_SPLIT;
   if (forced_kernel() != 0) pl.kernel = forced_kernel();
+  if (pl.kernel == MOE_W4A16_KERNEL_SPLIT && layout == MOE_W4A16_LAYOUT_CONTIGUOUS)
+    pl.kernel = MOE_W4A16_KERNEL_PREFILL;
   if (pl.kernel == MOE_W4A16_KERNEL_DECODE)
     pl.block_m = tok_e <= kDecodeSmallTokE ? kDecodeRowsSmall : kDecodeRows;
   else if (pl.kernel == MOE_W4A16_KERNEL_SPLIT)
@@ -743,7 +750,20 @@ moe_w4a16_status moe_w4a16_masked(const uint16_t* a3, int num_experts, int max_m
   p.max_m = max_m;
   p.row_ids = row_ids;
   p.c_rows = p.a_rows;
-  return run_gemm(p, pl.kernel, num_tokens, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (pl.kernel == MOE_W4A16_KERNEL_SPLIT) {
+    // the per-expert split: experts with at most kSplitRows rows on the decode kernel, the others on the
+    // tcgen05 kernel, both reading the experts' rows where they are; the fused combine needs all of a
+    // token's rows in one kernel, so a combining call stays on the tcgen05 family
+    if (flags & MOE_W4A16_FLAG_COMBINE) return run_gemm(p, MOE_W4A16_KERNEL_PREFILL, num_tokens, s);
+    GemmParams q = p;
+    p.side = 1;
+    moe_w4a16_status st2 = run_gemm(p, MOE_W4A16_KERNEL_DECODE, num_tokens, s);
+    if (st2 != MOE_W4A16_OK) return st2;
+    q.side = 2;
+    return run_gemm(q, MOE_W4A16_KERNEL_PREFILL, num_tokens, s);
+  }
+  return run_gemm(p, pl.kernel, num_tokens, s);
 }
 
 }  // extern "C"

@@ -81,6 +81,8 @@ struct GemmParams {
   // masked
   const int32_t* masked_m;
   int max_m;
+  int side;                  // masked split: 0 every expert, 1 only experts with at most kSplitRows rows (the
+                             // decode kernel's side), 2 only the others (the tcgen05 kernel's side)
 
   // combine
   const int32_t* row_ids;    // contiguous / masked: flat id of a layout row

@@ -184,6 +184,8 @@ __device__ __forceinline__ void masked_prefix_warp(const GemmParams& p, int rows
         set_error(p.err, MOE_W4A16_ERR_CAPACITY);
         m = p.max_m;
       }
+      // a split call: each kernel takes only its side's experts (the other side's get no blocks)
+      if ((p.side == 1 && m > kSplitRows) || (p.side == 2 && m <= kSplitRows)) m = 0;
       nb = (m + rows - 1) / rows;
     }
     int v = nb;
