@@ -18,6 +18,7 @@ the 129 MB L2), max over ranks. Multi-GPU runs are independent replicas.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -51,13 +52,16 @@ WORKLOAD_ALIASES = {
     "decode_down_combine": ("decode_down_combine", "indexed"),
     "tiny_indexed": ("tiny_indexed", "indexed"),
     "tp8_decode_gate_up_masked": ("tp8_decode_gate_up", "masked"),
+    # a crossover sweep point in the masked layout, budget above its hottest expert (1428 rows)
+    "sweep_gate_up_t1536_zipf_masked": ("sweep_gate_up_t1536_zipf", "masked", 1440),
 }
 
 
 def resolve(name: str):
     if name in WORKLOAD_ALIASES:
-        base, layout = WORKLOAD_ALIASES[name]
-        return S.get_workload(base), layout
+        base, layout, *max_m = WORKLOAD_ALIASES[name]
+        wl = S.get_workload(base)
+        return (dataclasses.replace(wl, max_m=max_m[0]) if max_m else wl), layout
     return S.get_workload(name), "indexed"
 
 
@@ -286,6 +290,10 @@ class OurArm:
             if layout == "masked":
                 self.max_m = wl.max_m
                 self.expected_m = max(1, int(self.counts[self.counts > 0].mean())) if self.e_active else 1
+                # a masked call picks its family itself from expected_m (the split per expert included)
+                mk = M.plan(M.LAYOUT_MASKED, t, k, e, n, kd, expected_m=self.expected_m).kernel
+                self.kernel_family = {M.KERNEL_DECODE: "decode", M.KERNEL_PREFILL: "prefill",
+                                      M.KERNEL_SPLIT: "split"}.get(mk, str(mk))
                 self.a3 = torch.empty((e, self.max_m, kd), dtype=torch.bfloat16, device=dev)
                 out_rows = e * self.max_m       # flat masked output
                 self.out = torch.empty((out_rows, n), dtype=torch.bfloat16, device=dev)
@@ -668,7 +676,8 @@ def roofline_of(arm, dom_us: float, peaks, peaks_src: str):
 # gate_up schedule sweep.
 REGIMES = (["decode_gate_up", "decode_gate_up_masked", "decode_down_combine", "tp8_decode_gate_up",
             "prefill_ffn_contiguous"]
-           + [f"sweep_gate_up_t{t}_{skew}" for t in S.SWEEP_TOKENS for skew in ("uniform", "zipf")])
+           + [f"sweep_gate_up_t{t}_{skew}" for t in S.SWEEP_TOKENS for skew in ("uniform", "zipf")]
+           + ["sweep_gate_up_t1536_zipf_masked"])
 
 
 # decode workloads also timed as align + GEMM (two launches) beside the one-launch routed call
@@ -818,7 +827,6 @@ def main(argv=None):
     wl, layout = resolve(args.workload)
     custom = bool(args.tokens or args.experts or args.layout or args.block_m)
     if args.tokens or args.experts:
-        import dataclasses
         t = args.tokens or wl.num_tokens
         e = args.experts or wl.num_experts
         wl = dataclasses.replace(wl, name=f"{wl.name}_t{t}_e{e}", num_tokens=t, num_experts=e,
