@@ -832,7 +832,6 @@ def main(argv=None):
         wl = dataclasses.replace(wl, name=f"{wl.name}_t{t}_e{e}", num_tokens=t, num_experts=e,
                                  hot_experts=min(wl.hot_experts, e))
     if args.layout:
-        import dataclasses
         layout = args.layout
         if layout == "masked" and args.max_m:
             wl = dataclasses.replace(wl, max_m=args.max_m)
