@@ -355,7 +355,10 @@ class OurArm:
         h = f.gate_up(a_in, route)
         if ev:
             ev[1].record()
-        return f.down(h, route, self.wts, self.out)
+        out = f.down(h, route, self.wts, self.out)
+        if ev and len(ev) > 2:
+            ev[2].record()
+        return out
 
     def flush_l2(self):
         """Writes a buffer twice the L2 size on the current stream (evicts the previous step's lines)."""
@@ -615,7 +618,9 @@ def time_steps(arm, steps: int, stream, sampler=None):
     import w4a16_int4_mixture_grouped_gb300 as M
     dev = arm.dev
     flush = needs_l2_flush(arm.weight_bytes)
-    dom = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    # FFN steps: a third event after the down GEMM + combine call (the pages sum gate_up and down)
+    n_ev = 3 if getattr(arm, "kind", "") == "ffn" else 2
+    dom = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(n_ev)) for _ in range(steps)]
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
@@ -635,8 +640,20 @@ def time_steps(arm, steps: int, stream, sampler=None):
         sampler.mark(w0, time.perf_counter())
     launches = M.launch_count() - launches0
     total_ms = sum(a.elapsed_time(b) for a, b in step_ev) if flush else t0.elapsed_time(t1)
-    dom_us = float(np.mean([a.elapsed_time(b) for a, b in dom])) * 1e3
+    dom_us = float(np.mean([d[0].elapsed_time(d[1]) for d in dom])) * 1e3
+    if n_ev == 3:
+        arm.down_combine_us = float(np.mean([d[1].elapsed_time(d[2]) for d in dom])) * 1e3
     return total_ms, dom_us, launches
+
+
+def ffn_kernels(arm, gate_up_us: float):
+    """An FFN step's GEMM calls, each timed by events around its own call: gate_up (with SwiGLU), the down GEMM
+    call (which also launches the combine pass over the staged rows), and their sum, the pages' convention of
+    summing the gate_up and down kernels."""
+    return {"gate_up_us": gate_up_us, "down_with_combine_us": arm.down_combine_us,
+            "sum_us": gate_up_us + arm.down_combine_us,
+            "what": "events around the gate_up call and around the down call; the down call is the down GEMM "
+                    "followed by the combine pass it launches"}
 
 
 def keep_busy(arm, seconds: float):
@@ -743,6 +760,8 @@ def measure_regimes(names, dev, steps: int, warmup: int, peaks, peaks_src, sampl
         rec["roofline"]["traffic"] = traffic
         if name == "decode_gate_up":
             rec["host_overhead"] = host_overhead(arm)
+        if getattr(arm, "down_combine_us", None) is not None:
+            rec["ffn_kernels"] = ffn_kernels(arm, dom_us)
         if getattr(arm, "routed", False) and name in TWO_LAUNCH_TOO:
             # the same workload as align + GEMM (two launches): its GEMM alone against the roofline
             del arm
@@ -906,6 +925,8 @@ def main(argv=None):
         "clocks": None,
         "gpu_launches": int(launches),
     }
+    if getattr(arm, "down_combine_us", None) is not None:
+        line["ffn_kernels"] = ffn_kernels(arm, dom_us)
     del arm
     torch.cuda.empty_cache()
     if not args.no_regimes and not custom and args.workload == "prefill_ffn":
