@@ -74,3 +74,20 @@ def test_regimes_cover_decode_and_every_sweep_point():
             assert f"sweep_gate_up_t{t}_{skew}" in names
     for n in names:
         B.resolve(n)
+
+
+def test_masked_workloads_budget_covers_their_hottest_expert():
+    """Every masked workload the bench times holds its hottest expert's rows within its row budget (else the call
+    would record a capacity error instead of a result), and the masked sweep point is a split call (expected_m, the
+    mean rows of its active experts, between 24 and 127)."""
+    import numpy as np
+    for name, alias in B.WORKLOAD_ALIASES.items():
+        wl, layout = B.resolve(name)
+        if layout != "masked":
+            continue
+        ids, _ = S.routing(wl)
+        counts = np.bincount(ids.reshape(-1), minlength=wl.num_experts)
+        assert wl.max_m >= counts.max(), name
+        if name.startswith("sweep_"):
+            expected_m = int(counts[counts > 0].mean())
+            assert 24 <= expected_m < 128, (name, expected_m)
