@@ -49,7 +49,8 @@ const DeviceInfo& device_info(int device) {
 // family is faster at 11 rows per expert (1.49 vs 2.12 ms) and the tcgen05
 // family at 32 (2.15 vs 2.92 ms), where 32-row decode blocks start to split
 // experts and stream their weights twice. Indexed calls between kSplitMinTokE and
-// kSplitMaxTokE take the per-expert split instead (the same rule per expert).
+// kSplitMaxTokE, and masked calls between kDecodeMaxTokE and kSplitMaxTokE, take the
+// per-expert split instead (the same rule per expert).
 constexpr int kDecodeMaxTokE = 24;
 // Average routed rows per expert up to which decode row blocks hold 16 rows
 // (three CTAs per SM); above it 32 (fewer blocks per loaded expert).
@@ -63,9 +64,9 @@ static bool log_enabled() {
   return on;
 }
 
-// MOE_W4A16_FORCE_KERNEL=decode|prefill overrides the family of the grouped
-// (contiguous / masked) entry points; read on every plan call and folded into
-// the memo key.
+// MOE_W4A16_FORCE_KERNEL=decode|prefill|split overrides the family the plan proposes
+// (the grouped entry points follow it; split is prefill for contiguous calls); read on
+// every plan call and folded into the memo key.
 static int forced_kernel() {
   const char* v = std::getenv("MOE_W4A16_FORCE_KERNEL");
   if (v == nullptr) return 0;
